@@ -1,0 +1,169 @@
+/*
+ * libkvarn -- the KVarN KV-cache codec on one GB300 GPU (sm_103a).
+ *
+ * The method (KVarN, arXiv:2606.03458) stores the KV cache of each attention head as
+ * 128-token x 128-channel tiles. On write, a completed tile is rotated over its channels by an
+ * orthonormal Hadamard matrix, normalised on both axes by alternating token/channel
+ * standard-deviation normalisation in the log domain (Sinkhorn-Knopp style), and round-to-nearest
+ * quantised to 2-bit codes (4-bit keys under the "kvarn_k4v2_g128" preset) with, per 128-element
+ * group, two FP8 scales and one FP16 zero-point.  On read, attention consumes the packed cache.
+ *
+ * Sources (web pages describing the paper; cited by page and section):
+ *   [paperlayer]  "KVarN: Variance-Normalized KV-Cache Quantization Mitigates Error Accumulation
+ *                 in Reasoning Tasks", paperlayer.ai source-linked summary of arXiv v1.
+ *   [dimensionstp] "KVarN: ... Review", dimensionstp.github.io study notes.
+ *   [agihunt]     agihunt.info summary of arXiv:2606.03458.
+ *   [pheeree]     pheeree.github.io blog post on KVarN (quotes the paper's sections verbatim).
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device; the caller owns them.
+ *     The library never allocates or frees memory and never synchronises the stream; work is
+ *     enqueued on `stream` (NULL = the legacy default stream).
+ *   - Arguments are validated on the host before anything is enqueued. On any error the call
+ *     returns a non-zero kvarn_status, enqueues nothing and leaves every output untouched;
+ *     kvarn_last_error() then describes the problem (thread-local text).
+ *   - A launch failure returns KVARN_ERR_CUDA (the CUDA error is consumed with cudaGetLastError).
+ *   - Head dimension and tile length are fixed at 128. Every pointer must be 16-byte aligned.
+ *
+ * Packed tile format (one 128-token x 128-channel tile of one head; all little-endian)
+ *   Tile axes: t = token (0..127), j = channel (0..127).  Y = X * H is the rotated tile, where
+ *   H[i][j] = (-1)^popcount(i & j) / sqrt(128) (Sylvester order, orthonormal and symmetric)
+ *   [paperlayer, "2 Preliminaries" and "A Hadamard Transform Arrangement"].
+ *   Groups of 128 elements follow KIVI [paperlayer, "2 Preliminaries"]: for K a group is one
+ *   channel (its 128 tokens); for V a group is one token (its 128 channels).  The "other axis"
+ *   is the remaining one (K: token, V: channel).
+ *   codes : 16*b bytes per token row (b = bits), rows in token order.  The row is cut into 16
+ *           little-endian lanes of b bytes; the code of channel j = 16*i + h (h = j mod 16,
+ *           i = j div 16) sits in lane h at bits [b*i, b*i + b).
+ *           2-bit tile: 4096 bytes; 4-bit tile: 8192 bytes.
+ *   params: 512 bytes per tile:
+ *           [  0,128) S1[g]  FP8 E4M3 group scale, indexed by group
+ *           [128,256) s2[o]  FP8 E4M3 other-axis scale, indexed by the other axis
+ *           [256,512) Z[g]   FP16 zero-point, indexed by group
+ *   tile_scale: one float32 per tile, g = a power of two that keeps S1 and Z inside their formats
+ *           (the per-tile factor this library adds; 32 bits per 16384 elements).
+ *   Dequantised (rotated basis):  Yhat[t][j] = g * s2[o] * (S1[grp] * code[t][j] + Z[grp]).
+ *   Storage: b + (8 + 8 + 16)/128 + 32/16384 bits per element = 2.2520 (b=2), 4.2520 (b=4);
+ *   the paper states 2.25 bits/element for 2-bit codes with two FP8 scales and one FP16
+ *   zero-point per 128-element group [paperlayer, "D Experimental details"].
+ */
+#ifndef KVARN_H
+#define KVARN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVARN_HEAD_DIM 128
+#define KVARN_TILE_TOKENS 128
+#define KVARN_PARAM_BYTES 512
+
+/* Compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* kvarn_stream_t;
+
+typedef enum {
+    KVARN_OK = 0,
+    KVARN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or enum is out of range */
+    KVARN_ERR_UNSUPPORTED = 2, /* a valid but unimplemented combination (e.g. 3-bit codes) */
+    KVARN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    KVARN_ERR_WORKSPACE = 4    /* the workspace passed is smaller than required */
+} kvarn_status;
+
+/* Which cache a tile belongs to; selects the group axis (K: channel, V: token). */
+typedef enum { KVARN_KIND_K = 0, KVARN_KIND_V = 1 } kvarn_kind;
+
+/* Flags for ablations: skip the Hadamard rotation and/or the variance normalisation.
+ * With both set the codec is plain asymmetric RTN per channel (K) / per token (V), i.e. KIVI's
+ * grouping [paperlayer, "5 Related Work"], with the scale stored as FP8 times the tile factor. */
+#define KVARN_FLAG_NO_ROTATE 1u
+#define KVARN_FLAG_NO_NORMALIZE 2u
+
+typedef struct {
+    int32_t k_bits;         /* 2 or 4 */
+    int32_t v_bits;         /* 2 or 4 */
+    int32_t sinkhorn_iters; /* 0..64; the paper uses 8 [paperlayer, "4 Experiments", Efficiency] */
+    uint32_t flags;         /* KVARN_FLAG_* */
+} kvarn_config;
+
+/* Fill *out from a preset name.  "kvarn_k4v2_g128": 4-bit K, 2-bit V, group 128, 8 iterations
+ * (the shipped preset [dimensionstp, "3-1 Overview"]); "kvarn_k2v2_g128": all 2-bit (the
+ * paper's experimental setting [paperlayer, "D Experimental details"]).
+ * Returns KVARN_ERR_INVALID_ARG for a NULL pointer or an unknown name. */
+kvarn_status kvarn_config_from_preset(const char* name, kvarn_config* out);
+
+/* Bytes of packed codes per tile for b-bit codes (16*128*b: 4096 for b=2, 8192 for b=4);
+ * 0 for an unsupported b. */
+size_t kvarn_tile_code_bytes(int bits);
+
+/* Bytes of per-tile parameters (S1, s2, Z): 512.  The float tile_scale is stored apart. */
+size_t kvarn_tile_param_bytes(void);
+
+/* Encode n_tiles completed tiles of one cache kind [paperlayer, "3 Methods"; agihunt, pipeline
+ * paragraph: rotate -> dual-axis variance normalisation -> RTN].
+ *   x_bf16     : [n_tiles][128 tokens][128 channels] bfloat16, token-major (post-RoPE K or V).
+ *   codes      : [n_tiles][kvarn_tile_code_bytes(bits)] output.
+ *   params     : [n_tiles][512] output.
+ *   tile_scale : [n_tiles] float32 output.
+ * bits = cfg->k_bits for KVARN_KIND_K, cfg->v_bits for KVARN_KIND_V.  n_tiles == 0 is a no-op.
+ * Errors: NULL/misaligned pointer, n_tiles < 0, bits not in {2,4}, iterations outside 0..64. */
+kvarn_status kvarn_encode_blocks(const kvarn_config* cfg, kvarn_kind kind, const void* x_bf16,
+                                 int64_t n_tiles, void* codes, void* params, float* tile_scale,
+                                 kvarn_stream_t stream);
+
+/* Dequantise n_tiles packed tiles to float32 [n_tiles][128][128] (token-major).
+ * original_basis = 0 returns Yhat (rotated basis); 1 returns Yhat * H, the estimate of the
+ * input tile [paperlayer, "I KVarN Dequantization Overhead": both scales are applied in one
+ * pass].  With KVARN_FLAG_NO_ROTATE the two are the same.  Errors as for encode. */
+kvarn_status kvarn_dequant(const kvarn_config* cfg, kvarn_kind kind, const void* codes,
+                           const void* params, const float* tile_scale, int64_t n_tiles,
+                           int original_basis, float* out, kvarn_stream_t stream);
+
+/* Bytes of device workspace kvarn_decode_attention needs for this shape (split-K partials).
+ * Returns 0 for an invalid shape. */
+size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int Hkv,
+                                   int max_tiles);
+
+/* Decode attention, one query per sequence, grouped-query heads, over the packed cache
+ * [dimensionstp, "4-2 Training strategy": the quantised cache is restored at attention read
+ * time; paperlayer, "A Hadamard Transform Arrangement": the query is rotated by the same
+ * head-wise Hadamard after RoPE so keys stay in the rotated basis].
+ *   q_bf16      : [B][Hq][128] bfloat16 queries (original basis).
+ *   k_codes, k_params, k_scale : K tile pool (bits = cfg->k_bits); v_*: V tile pool.  The two
+ *                 pools are indexed by the same tile id.
+ *   block_table : [B][Hkv][max_tiles] int32 tile ids; entry i of (b, kv head) is the tile
+ *                 holding tokens [128 i, 128 i + 128) of that sequence.
+ *   seq_lens    : [B] int32 device array, tokens of context per sequence (0 allowed).
+ *   seq_lens_host: optional [B] host copy; when given, every length is checked against
+ *                 128*max_tiles + 127 before launch (device lengths are clamped in any case).
+ *   k_tail_bf16, v_tail_bf16 : [B][Hkv][128][128] bfloat16, original basis; tokens
+ *                 [128*floor(L/128), L) of sequence b are rows 0 .. L mod 128 - 1.
+ *   softmax_scale: multiplies q.k before the softmax.
+ *   workspace   : at least kvarn_decode_workspace_size(...) bytes of device memory.
+ *   out         : [B][Hq][128] float32 attention output (original basis); a sequence of
+ *                 length 0 gets zeros.
+ * Hq must be a multiple of Hkv with Hq/Hkv in {1, 2, 4, 8}.  Tile ids are not range-checked on
+ * the device: they must index the pools the caller passes. */
+kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
+                                    int Hkv, const void* k_codes, const void* k_params,
+                                    const float* k_scale, const void* v_codes,
+                                    const void* v_params, const float* v_scale,
+                                    const int32_t* block_table, int max_tiles,
+                                    const int32_t* seq_lens, const int32_t* seq_lens_host,
+                                    const void* k_tail_bf16, const void* v_tail_bf16,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    float* out, kvarn_stream_t stream);
+
+/* Static text for a status code. */
+const char* kvarn_status_string(kvarn_status status);
+
+/* Thread-local description of the last error returned on this thread ("" if none). */
+const char* kvarn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H */
