@@ -1,0 +1,200 @@
+"""Python binding of libkvarn, the KVarN KV-cache codec for GB300 (sm_103a).
+
+Argument marshalling only: every step of the codec runs in the CUDA kernels of libkvarn.so.  The
+functions keep the C names and order of arguments; tensors are torch CUDA tensors (their
+data_ptr() is passed) and the stream defaults to torch's current stream.  There is no fallback:
+if the shared library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import synthetic  # noqa: F401  (seeded workload generators)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvarn.so")
+
+KVARN_KIND_K = 0
+KVARN_KIND_V = 1
+KVARN_FLAG_NO_ROTATE = 1
+KVARN_FLAG_NO_NORMALIZE = 2
+PARAM_BYTES = 512
+TILE = 128
+
+
+class KvarnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class kvarn_config(ctypes.Structure):
+    _fields_ = [("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32),
+                ("sinkhorn_iters", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+    def __repr__(self):
+        return (f"kvarn_config(k_bits={self.k_bits}, v_bits={self.v_bits}, "
+                f"sinkhorn_iters={self.sinkhorn_iters}, flags={self.flags})")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "kvarn_config_from_preset": (_i32, [ctypes.c_char_p, ctypes.POINTER(kvarn_config)]),
+    "kvarn_tile_code_bytes": (_sz, [_i32]),
+    "kvarn_tile_param_bytes": (_sz, []),
+    "kvarn_encode_blocks": (_i32, [ctypes.POINTER(kvarn_config), _i32, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "kvarn_dequant": (_i32, [ctypes.POINTER(kvarn_config), _i32, _vp, _vp, _vp, _i64, _i32, _vp, _vp]),
+    "kvarn_decode_workspace_size": (_sz, [ctypes.POINTER(kvarn_config), _i32, _i32, _i32, _i32]),
+    "kvarn_decode_attention": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
+                                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
+                                      ctypes.c_float, _vp, _sz, _vp, _vp]),
+    "kvarn_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
+    "kvarn_status_string": (ctypes.c_char_p, [_i32]),
+    "kvarn_last_error": (ctypes.c_char_p, []),
+}
+
+
+def load(path: str | None = None):
+    """Load libkvarn.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkvarn.so not found at {path}: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load()
+        raise KvarnError(status, lib.kvarn_last_error().decode() or lib.kvarn_status_string(status).decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need(t, dtype, numel, name):
+    if not isinstance(t, torch.Tensor):
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+
+
+def kvarn_config_from_preset(name: str) -> kvarn_config:
+    cfg = kvarn_config()
+    _check(load().kvarn_config_from_preset(name.encode(), ctypes.byref(cfg)))
+    return cfg
+
+
+def make_config(k_bits=2, v_bits=2, sinkhorn_iters=8, flags=0) -> kvarn_config:
+    return kvarn_config(k_bits, v_bits, sinkhorn_iters, flags)
+
+
+def kvarn_tile_code_bytes(bits: int) -> int:
+    return int(load().kvarn_tile_code_bytes(bits))
+
+
+def kvarn_tile_param_bytes() -> int:
+    return int(load().kvarn_tile_param_bytes())
+
+
+def kvarn_encode_blocks(cfg: kvarn_config, kind: int, x, codes, params, tile_scale, stream=None,
+                        n_tiles: int | None = None):
+    """x: [n, 128, 128] bf16 -> codes [n, code_bytes] u8, params [n, 512] u8, tile_scale [n] f32."""
+    if n_tiles is None:
+        n_tiles = x.shape[0]
+    bits = cfg.k_bits if kind == KVARN_KIND_K else cfg.v_bits
+    _need(x, torch.bfloat16, n_tiles * TILE * TILE, "x")
+    _need(codes, torch.uint8, n_tiles * TILE * 16 * bits, "codes")
+    _need(params, torch.uint8, n_tiles * PARAM_BYTES, "params")
+    _need(tile_scale, torch.float32, n_tiles, "tile_scale")
+    _check(load().kvarn_encode_blocks(ctypes.byref(cfg), kind, _ptr(x), n_tiles, _ptr(codes),
+                                      _ptr(params), _ptr(tile_scale), _stream(stream)))
+
+
+def kvarn_dequant(cfg: kvarn_config, kind: int, codes, params, tile_scale, out, original_basis=1,
+                  stream=None, n_tiles: int | None = None):
+    """Packed tiles -> float32 [n, 128, 128]."""
+    if n_tiles is None:
+        n_tiles = tile_scale.shape[0]
+    bits = cfg.k_bits if kind == KVARN_KIND_K else cfg.v_bits
+    _need(codes, torch.uint8, n_tiles * TILE * 16 * bits, "codes")
+    _need(params, torch.uint8, n_tiles * PARAM_BYTES, "params")
+    _need(tile_scale, torch.float32, n_tiles, "tile_scale")
+    _need(out, torch.float32, n_tiles * TILE * TILE, "out")
+    _check(load().kvarn_dequant(ctypes.byref(cfg), kind, _ptr(codes), _ptr(params),
+                                _ptr(tile_scale), n_tiles, int(original_basis), _ptr(out),
+                                _stream(stream)))
+
+
+def kvarn_decode_workspace_size(cfg: kvarn_config, B: int, Hq: int, Hkv: int, max_tiles: int) -> int:
+    return int(load().kvarn_decode_workspace_size(ctypes.byref(cfg), B, Hq, Hkv, max_tiles))
+
+
+def kvarn_decode_attention(cfg: kvarn_config, q, Hkv: int, k_codes, k_params, k_scale, v_codes,
+                           v_params, v_scale, block_table, seq_lens, k_tail, v_tail,
+                           softmax_scale: float, workspace, out, seq_lens_host=None, stream=None):
+    """q: [B, Hq, 128] bf16; block_table: [B, Hkv, max_tiles] int32; seq_lens: [B] int32 (device);
+    tails: [B, Hkv, 128, 128] bf16; out: [B, Hq, 128] float32."""
+    B, Hq = q.shape[0], q.shape[1]
+    max_tiles = block_table.shape[-1]
+    _need(q, torch.bfloat16, B * Hq * TILE, "q")
+    _need(block_table, torch.int32, B * Hkv * max_tiles, "block_table")
+    _need(seq_lens, torch.int32, B, "seq_lens")
+    _need(k_tail, torch.bfloat16, B * Hkv * TILE * TILE, "k_tail")
+    _need(v_tail, torch.bfloat16, B * Hkv * TILE * TILE, "v_tail")
+    _need(out, torch.float32, B * Hq * TILE, "out")
+    host = None
+    if seq_lens_host is not None:
+        arr = (ctypes.c_int32 * B)(*[int(v) for v in seq_lens_host])
+        host = ctypes.cast(arr, ctypes.c_void_p)
+    ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
+    _check(load().kvarn_decode_attention(
+        ctypes.byref(cfg), _ptr(q), B, Hq, Hkv, _ptr(k_codes), _ptr(k_params), _ptr(k_scale),
+        _ptr(v_codes), _ptr(v_params), _ptr(v_scale), _ptr(block_table), max_tiles, _ptr(seq_lens),
+        host, _ptr(k_tail), _ptr(v_tail), float(softmax_scale), _ptr(workspace), ws_bytes,
+        _ptr(out), _stream(stream)))
+
+
+def kvarn_device_error() -> int:
+    v = ctypes.c_uint32(0)
+    _check(load().kvarn_device_error(ctypes.byref(v)))
+    return int(v.value)
+
+
+def kvarn_status_string(status: int) -> str:
+    return load().kvarn_status_string(status).decode()

@@ -1,0 +1,474 @@
+// KVarN tile encoder: Hadamard rotation -> dual-axis variance normalisation -> scale split ->
+// round-to-nearest -> bit packing, one 128x128 bf16 tile at a time per CTA.
+//
+// Method: KVarN (arXiv:2606.03458) as summarised on paperlayer.ai ("3 Methods": channel-wise
+// Hadamard rotation and online variance scaling across both the channel and the token
+// dimension; "D Experimental details": 2-bit codes, two FP8 scales and one FP16 zero-point per
+// 128-element group) and agihunt.info (pipeline: rotate, then Sinkhorn-Knopp style alternating
+// token/channel variance normalisation, then RTN; normalisation factors absorbed into the
+// group scale).
+//
+// Design (GB300): persistent grid, one CTA per SM; the bf16 tile (32 KB, contiguous) arrives by a
+// 1-D TMA bulk copy into a double-buffered shared-memory slot while the previous tile is being
+// processed.  The rotation is two register passes around one shared-memory transpose
+// (H_128 = (H_8 x I_16)(I_8 x H_16)).  Each thread then owns 8 tokens x 8 channels of the rotated
+// tile, Y and Y^2 held as float2 pairs, so every statistics update of the Sinkhorn iteration is
+// one packed FFMA2 per element: token sums reduce over 16 lanes by shuffles, channel sums over
+// the two half-warps by a shuffle and over the 8 warps through shared memory.
+#include <climits>
+
+#include "kvarn_common.cuh"
+#include "kvarn_internal.h"
+
+namespace kvarn {
+
+// Set by the encoder when a TMA copy never completes (bounded wait); read by kvarn_device_error.
+__device__ unsigned int g_encode_error = 0;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = 8;
+
+struct EncodeSmem {
+    __nv_bfloat16 xs[2][kTile * kTile];    // TMA destination, double-buffered (64 KB)
+    float ys[kTile * kYStride];            // FWHT staging (72 KB)
+    float2 red[kWarps][4][32];             // cross-warp partial sums (8 KB)
+    float2 aa[kTile];                      // (1/c, 1/c^2) per channel
+    float cfac[kTile];                     // channel factor c
+    float logf_[kTile];                    // log of the other-axis factor
+    float grp_min[kTile];
+    float grp_scale[kTile];
+    float grp_z[kTile];                    // zero-point (value of the FP16 code)
+    float grp_inv_s1[kTile];               // 1 / S1 (0 where S1 = 0)
+    float oth_inv_s2[kTile];               // 1 / s2 along the other axis
+    float bred[kWarps];                    // block reductions
+    float bcast[4];
+    alignas(16) uint8_t params[KVARN_PARAM_BYTES];
+    alignas(16) uint32_t codes[kTile * 16];  // packed rows (up to 8 KB)
+    alignas(8) uint64_t bar[2];
+};
+
+__device__ __forceinline__ float block_sum_128(EncodeSmem& sm, float v, int tid) {
+    // sum of v over threads 0..127 (4 warps); result broadcast through shared memory
+    v = warp_sum(v);
+    if (tid < 128 && (tid & 31) == 0) sm.bred[tid >> 5] = v;
+    __syncthreads();
+    float r = sm.bred[0] + sm.bred[1] + sm.bred[2] + sm.bred[3];
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ float block_max_128(EncodeSmem& sm, float v, int tid) {
+    v = warp_max(v);
+    if (tid < 128 && (tid & 31) == 0) sm.bred[tid >> 5] = v;
+    __syncthreads();
+    float r = fmaxf(fmaxf(sm.bred[0], sm.bred[1]), fmaxf(sm.bred[2], sm.bred[3]));
+    __syncthreads();
+    return r;
+}
+
+// Power-of-two tile factor: largest S/g in (128, 256] unless |m|/g would pass 32768.
+__device__ __forceinline__ float tile_factor(float s_max, float m_max) {
+    int e = INT_MIN;
+    if (s_max > 0.f) e = ceil_log2(s_max) - 8;
+    if (m_max > 0.f) e = max(e, ceil_log2(m_max) - 15);
+    return e == INT_MIN ? 1.f : ldexpf(1.f, e);
+}
+
+template <int BITS, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ codes_out,
+              uint8_t* __restrict__ params_out, float* __restrict__ scale_out, int iters,
+              int rotate, int normalize) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
+    constexpr int kLevels = (1 << BITS) - 1;
+    constexpr uint32_t kTileBytes = kTile * kTile * 2;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int h = lane & 15;                 // channel lane: channels h + 16 i
+    const int tsub = lane >> 4;
+    const int tg = 2 * warp + tsub;          // token group: tokens tg + 16 k
+
+    if (tid == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            int64_t t = blockIdx.x + (int64_t)b * gridDim.x;
+            if (t < n_tiles) {
+                mbar_expect_tx(&sm.bar[b], kTileBytes);
+                bulk_g2s(sm.xs[b], x + t * kTile * kTile, kTileBytes, &sm.bar[b]);
+            }
+        }
+    }
+
+    int local = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const bool ok_data = mbar_wait(&sm.bar[buf], (local >> 1) & 1, &g_encode_error);
+        const __nv_bfloat16* xs = sm.xs[buf];
+
+        // ---- rotation pass 1: H_16 over channel bits 0..3, 16 contiguous channels per item ----
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int idx = tid + kThreads * it;
+            const int t = idx >> 3, c = idx & 7;
+            float v[16];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int half = hh ^ ((c >> 2) & 1);  // bank-conflict-free order
+                uint4 raw = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * half);
+                const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    float2 f = __bfloat1622float2(p2[m]);
+                    v[8 * half + 2 * m] = f.x;
+                    v[8 * half + 2 * m + 1] = f.y;
+                }
+            }
+            if (rotate) fwht_regs<16>(v);
+            float* dst = sm.ys + t * kYStride + 16 * c;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int qq = (q + (c >> 1)) & 3;
+                *reinterpret_cast<float4*>(dst + 4 * qq) =
+                    make_float4(v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
+            }
+        }
+        __syncthreads();
+        // the bf16 slot is free again: prefetch the tile after next into it
+        if (tid == 0) {
+            int64_t nt = tile + 2 * (int64_t)gridDim.x;
+            if (nt < n_tiles) {
+                fence_proxy_async();
+                mbar_expect_tx(&sm.bar[buf], kTileBytes);
+                bulk_g2s(sm.xs[buf], x + nt * kTile * kTile, kTileBytes, &sm.bar[buf]);
+            }
+        }
+
+        // ---- rotation pass 2: H_8 over channel bits 4..6; thread keeps (Y, Y^2) ----
+        float2 yy[8][8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = tg + 16 * k;
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = sm.ys[t * kYStride + h + 16 * i];
+            if (rotate) {
+                fwht_regs<8>(v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] *= kInvSqrt128;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yy[k][i] = make_float2(v[i], v[i] * v[i]);
+        }
+
+        // ---- dual-axis variance normalisation ----
+        // token step:   r_t = std_j(Y_tj / c_j)   (lane owns token kown of its 8 for the update)
+        // channel step: c_j = std_t(Y_tj / r_t)
+        const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
+        float r_own = 1.f;
+        float2 aa[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) aa[i] = make_float2(1.f, 1.f);
+        if (tid < kTile) sm.cfac[tid] = 1.f;
+        const int n_it = normalize ? iters : 0;
+        for (int itn = 0; itn < n_it; ++itn) {
+            // token step
+            float2 acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                acc[k] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[k] = ffma2(yy[k][i], aa[i], acc[k]);
+            }
+            // transposing reduction over the 16 channel lanes
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool up = (h & 8) != 0;
+                float2 send = up ? acc[q] : acc[q + 4];
+                float2 keep = up ? acc[q + 4] : acc[q];
+                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 8);
+                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 8);
+                acc[q] = keep;
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const bool up = (h & 4) != 0;
+                float2 send = up ? acc[q] : acc[q + 2];
+                float2 keep = up ? acc[q + 2] : acc[q];
+                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 4);
+                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 4);
+                acc[q] = keep;
+            }
+            {
+                const bool up = (h & 2) != 0;
+                float2 send = up ? acc[0] : acc[1];
+                float2 keep = up ? acc[1] : acc[0];
+                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 2);
+                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 2);
+                keep.x += __shfl_xor_sync(0xffffffffu, keep.x, 1);
+                keep.y += __shfl_xor_sync(0xffffffffu, keep.y, 1);
+                const float mean = keep.x * (1.f / kTile);
+                const float ms = keep.y * (1.f / kTile);
+                const float var = ms - mean * mean;
+                if (var > kDegenerateRel * ms) r_own = sqrtf(var);
+            }
+            const float b_own = 1.f / r_own;
+            float2 bb[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int src = (lane & 16) | (((k >> 2) & 1) << 3) | (((k >> 1) & 1) << 2) | ((k & 1) << 1);
+                const float b = __shfl_sync(0xffffffffu, b_own, src);
+                bb[k] = make_float2(b, b * b);
+            }
+            // channel step
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[i] = ffma2(yy[k][i], bb[k], acc[i]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float2 send = tsub ? acc[q] : acc[q + 4];
+                float2 keep = tsub ? acc[q + 4] : acc[q];
+                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 16);
+                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 16);
+                sm.red[warp][q][lane] = keep;  // channel h + 16 (q + 4 tsub)
+            }
+            __syncthreads();
+            if (tid < kTile) {
+                const int j = tid, hj = j & 15, ij = j >> 4;
+                const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
+                float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    float2 p = sm.red[w][q][src_lane];
+                    s.x += p.x;
+                    s.y += p.y;
+                }
+                const float mean = s.x * (1.f / kTile);
+                const float ms = s.y * (1.f / kTile);
+                const float var = ms - mean * mean;
+                float c = sm.cfac[j];
+                if (var > kDegenerateRel * ms) c = sqrtf(var);
+                sm.cfac[j] = c;
+                const float a = 1.f / c;
+                sm.aa[j] = make_float2(a, a * a);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) aa[i] = sm.aa[h + 16 * i];
+        }
+
+        // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
+        // K: other axis = token (factor r); V: other axis = channel (factor c).
+        if (KIND == KVARN_KIND_K) {
+            if ((h & 1) == 0) sm.logf_[tg + 16 * kown] = logf(r_own);
+        } else {
+            if (tid < kTile) sm.logf_[tid] = logf(sm.cfac[tid]);
+        }
+        __syncthreads();
+        const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[tid] : 0.f, tid) * (1.f / kTile);
+        if (tid < kTile) {
+            float s2 = e4m3_value(e4m3_rn(expf(sm.logf_[tid] - mean_log)));
+            s2 = fminf(fmaxf(s2, 0.001953125f), 448.f);  // [2^-9, 448]
+            sm.params[128 + tid] = e4m3_rn(s2);
+            sm.oth_inv_s2[tid] = 1.f / s2;
+        }
+        __syncthreads();
+
+        // W = Y / s2, then per-group min / max
+        float gmin_own = 0.f, gmax_own = 0.f;  // V: this lane's token kown
+        if (KIND == KVARN_KIND_K) {
+            float2 mm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float inv = sm.oth_inv_s2[tg + 16 * k];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) yy[k][i].x *= inv;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float lo = yy[0][i].x, hi = yy[0][i].x;
+#pragma unroll
+                for (int k = 1; k < 8; ++k) {
+                    lo = fminf(lo, yy[k][i].x);
+                    hi = fmaxf(hi, yy[k][i].x);
+                }
+                mm[i] = make_float2(lo, hi);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float2 send = tsub ? mm[q] : mm[q + 4];
+                float2 keep = tsub ? mm[q + 4] : mm[q];
+                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 16));
+                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 16));
+                sm.red[warp][q][lane] = keep;
+            }
+            __syncthreads();
+            if (tid < kTile) {
+                const int j = tid, hj = j & 15, ij = j >> 4;
+                const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
+                float lo = sm.red[0][q][src_lane].x, hi = sm.red[0][q][src_lane].y;
+#pragma unroll
+                for (int w = 1; w < kWarps; ++w) {
+                    lo = fminf(lo, sm.red[w][q][src_lane].x);
+                    hi = fmaxf(hi, sm.red[w][q][src_lane].y);
+                }
+                sm.grp_min[j] = lo;
+                sm.grp_scale[j] = (hi - lo) / (float)kLevels;
+            }
+        } else {
+            float inv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) inv[i] = sm.oth_inv_s2[h + 16 * i];
+            float2 mm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float lo = 0.f, hi = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float w = yy[k][i].x * inv[i];
+                    yy[k][i].x = w;
+                    lo = i ? fminf(lo, w) : w;
+                    hi = i ? fmaxf(hi, w) : w;
+                }
+                mm[k] = make_float2(lo, hi);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool up = (h & 8) != 0;
+                float2 send = up ? mm[q] : mm[q + 4];
+                float2 keep = up ? mm[q + 4] : mm[q];
+                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 8));
+                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 8));
+                mm[q] = keep;
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const bool up = (h & 4) != 0;
+                float2 send = up ? mm[q] : mm[q + 2];
+                float2 keep = up ? mm[q + 2] : mm[q];
+                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 4));
+                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 4));
+                mm[q] = keep;
+            }
+            {
+                const bool up = (h & 2) != 0;
+                float2 send = up ? mm[0] : mm[1];
+                float2 keep = up ? mm[1] : mm[0];
+                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 2));
+                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 2));
+                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, keep.x, 1));
+                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, keep.y, 1));
+                gmin_own = keep.x;
+                gmax_own = keep.y;
+            }
+            if ((h & 1) == 0) {
+                const int t = tg + 16 * kown;
+                sm.grp_min[t] = gmin_own;
+                sm.grp_scale[t] = (gmax_own - gmin_own) / (float)kLevels;
+            }
+        }
+        __syncthreads();
+
+        // ---- tile factor g, group scale S1 (E4M3, rounded up) and zero-point Z (FP16) ----
+        const float s_max = block_max_128(sm, tid < kTile ? sm.grp_scale[tid] : 0.f, tid);
+        const float m_max = block_max_128(sm, tid < kTile ? fabsf(sm.grp_min[tid]) : 0.f, tid);
+        const float g = tile_factor(s_max, m_max);
+        const float inv_g = 1.f / g;  // exact: g is a power of two
+        if (tid < kTile) {
+            const uint8_t s1b = e4m3_up(sm.grp_scale[tid] * inv_g);
+            const float s1 = e4m3_value(s1b);
+            const __half zh = __float2half_rn(sm.grp_min[tid] * inv_g);
+            sm.params[tid] = s1b;
+            reinterpret_cast<__half*>(sm.params + 256)[tid] = zh;
+            sm.grp_z[tid] = __half2float(zh);
+            sm.grp_inv_s1[tid] = s1 > 0.f ? 1.f / s1 : 0.f;
+        }
+        __syncthreads();
+
+        // ---- codes and packing: lane h of token row t holds channels h + 16 i at bits BITS*i ----
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = tg + 16 * k;
+            uint32_t packed = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * i) : t;
+                const float u = (yy[k][i].x * inv_g - sm.grp_z[grp]) * sm.grp_inv_s1[grp];
+                int c = __float2int_rn(u);
+                c = min(max(c, 0), kLevels);
+                packed |= (uint32_t)c << (BITS * i);
+            }
+            if (BITS == 2)
+                reinterpret_cast<uint16_t*>(sm.codes)[t * 16 + h] = (uint16_t)packed;
+            else
+                sm.codes[t * 16 + h] = packed;
+        }
+        __syncthreads();
+
+        // ---- write out: codes (16-byte stores), params, tile factor ----
+        if (ok_data) {
+            constexpr int kCodeBytes = kTile * 16 * BITS;
+            uint4* dst = reinterpret_cast<uint4*>(codes_out + tile * kCodeBytes);
+            const uint4* src = reinterpret_cast<const uint4*>(sm.codes);
+#pragma unroll
+            for (int v = tid; v < kCodeBytes / 16; v += kThreads) dst[v] = src[v];
+            if (tid < KVARN_PARAM_BYTES / 16)
+                reinterpret_cast<uint4*>(params_out + tile * KVARN_PARAM_BYTES)[tid] =
+                    reinterpret_cast<const uint4*>(sm.params)[tid];
+            if (tid == 0) scale_out[tile] = g;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+size_t encode_smem_bytes() { return sizeof(EncodeSmem); }
+
+cudaError_t read_and_clear_device_error(unsigned int* out) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_encode_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_encode_error, &zero, sizeof(zero));
+    *out = v;
+    return e;
+}
+
+cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
+                          void* params, float* tile_scale, int iters, int rotate, int normalize,
+                          cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    const int grid = (int)(n_tiles < sms ? n_tiles : sms);
+    const size_t smem = sizeof(EncodeSmem);
+    auto run = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kThreads, smem, stream>>>(static_cast<const __nv_bfloat16*>(x), n_tiles,
+                                               static_cast<uint8_t*>(codes),
+                                               static_cast<uint8_t*>(params), tile_scale, iters,
+                                               rotate, normalize);
+        return cudaGetLastError();
+    };
+    if (bits == 2 && kind == KVARN_KIND_K) return run(encode_kernel<2, KVARN_KIND_K>);
+    if (bits == 2 && kind == KVARN_KIND_V) return run(encode_kernel<2, KVARN_KIND_V>);
+    if (bits == 4 && kind == KVARN_KIND_K) return run(encode_kernel<4, KVARN_KIND_K>);
+    return run(encode_kernel<4, KVARN_KIND_V>);
+}
+
+}  // namespace kvarn

@@ -1,0 +1,219 @@
+// libkvarn C-ABI: argument validation and kernel launches.  See include/kvarn.h for the contract.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "../../include/kvarn.h"
+#include "kvarn_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvarn_status fail(kvarn_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kvarn_status fail(kvarn_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kvarn_status ok() {
+    g_last_error.clear();
+    return KVARN_OK;
+}
+
+kvarn_status cuda_fail(cudaError_t e, const char* what) {
+    cudaGetLastError();  // consume
+    return fail(KVARN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+kvarn_status check_cfg(const kvarn_config* cfg) {
+    if (!cfg) return fail(KVARN_ERR_INVALID_ARG, "cfg is NULL");
+    if (cfg->k_bits != 2 && cfg->k_bits != 4)
+        return fail(KVARN_ERR_INVALID_ARG, "k_bits = %d; supported: 2, 4", cfg->k_bits);
+    if (cfg->v_bits != 2 && cfg->v_bits != 4)
+        return fail(KVARN_ERR_INVALID_ARG, "v_bits = %d; supported: 2, 4", cfg->v_bits);
+    if (cfg->sinkhorn_iters < 0 || cfg->sinkhorn_iters > 64)
+        return fail(KVARN_ERR_INVALID_ARG, "sinkhorn_iters = %d; allowed 0..64", cfg->sinkhorn_iters);
+    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATE | KVARN_FLAG_NO_NORMALIZE))
+        return fail(KVARN_ERR_INVALID_ARG, "unknown flag bits 0x%x", cfg->flags);
+    return KVARN_OK;
+}
+
+kvarn_status check_ptr(const void* p, size_t align, const char* name) {
+    if (!p) return fail(KVARN_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, align)) return fail(KVARN_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+    return KVARN_OK;
+}
+
+#define KV_TRY(expr)                     \
+    do {                                 \
+        kvarn_status _s = (expr);        \
+        if (_s != KVARN_OK) return _s;   \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+kvarn_status kvarn_config_from_preset(const char* name, kvarn_config* out) {
+    if (!name || !out) return fail(KVARN_ERR_INVALID_ARG, "name or out is NULL");
+    if (strcmp(name, "kvarn_k4v2_g128") == 0) {
+        *out = kvarn_config{4, 2, 8, 0u};
+        return ok();
+    }
+    if (strcmp(name, "kvarn_k2v2_g128") == 0) {
+        *out = kvarn_config{2, 2, 8, 0u};
+        return ok();
+    }
+    return fail(KVARN_ERR_INVALID_ARG, "unknown preset '%s' (known: kvarn_k4v2_g128, kvarn_k2v2_g128)", name);
+}
+
+size_t kvarn_tile_code_bytes(int bits) {
+    return (bits == 2 || bits == 4) ? (size_t)KVARN_TILE_TOKENS * 16 * bits : 0;
+}
+
+size_t kvarn_tile_param_bytes(void) { return KVARN_PARAM_BYTES; }
+
+kvarn_status kvarn_encode_blocks(const kvarn_config* cfg, kvarn_kind kind, const void* x_bf16,
+                                 int64_t n_tiles, void* codes, void* params, float* tile_scale,
+                                 kvarn_stream_t stream) {
+    KV_TRY(check_cfg(cfg));
+    if (kind != KVARN_KIND_K && kind != KVARN_KIND_V)
+        return fail(KVARN_ERR_INVALID_ARG, "kind = %d; expected KVARN_KIND_K or KVARN_KIND_V", (int)kind);
+    if (n_tiles < 0) return fail(KVARN_ERR_INVALID_ARG, "n_tiles = %lld < 0", (long long)n_tiles);
+    if (n_tiles == 0) return ok();
+    KV_TRY(check_ptr(x_bf16, 16, "x_bf16"));
+    KV_TRY(check_ptr(codes, 16, "codes"));
+    KV_TRY(check_ptr(params, 16, "params"));
+    KV_TRY(check_ptr(tile_scale, 4, "tile_scale"));
+    const int bits = kind == KVARN_KIND_K ? cfg->k_bits : cfg->v_bits;
+    cudaError_t e = kvarn::launch_encode(bits, (int)kind, x_bf16, n_tiles, codes, params, tile_scale,
+                                         cfg->sinkhorn_iters, !(cfg->flags & KVARN_FLAG_NO_ROTATE),
+                                         !(cfg->flags & KVARN_FLAG_NO_NORMALIZE), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "encode launch");
+    return ok();
+}
+
+kvarn_status kvarn_dequant(const kvarn_config* cfg, kvarn_kind kind, const void* codes,
+                           const void* params, const float* tile_scale, int64_t n_tiles,
+                           int original_basis, float* out, kvarn_stream_t stream) {
+    KV_TRY(check_cfg(cfg));
+    if (kind != KVARN_KIND_K && kind != KVARN_KIND_V)
+        return fail(KVARN_ERR_INVALID_ARG, "kind = %d; expected KVARN_KIND_K or KVARN_KIND_V", (int)kind);
+    if (n_tiles < 0 || n_tiles > 0x7fffffffLL)
+        return fail(KVARN_ERR_INVALID_ARG, "n_tiles = %lld outside 0..2^31-1", (long long)n_tiles);
+    if (original_basis != 0 && original_basis != 1)
+        return fail(KVARN_ERR_INVALID_ARG, "original_basis = %d; expected 0 or 1", original_basis);
+    if (n_tiles == 0) return ok();
+    KV_TRY(check_ptr(codes, 16, "codes"));
+    KV_TRY(check_ptr(params, 16, "params"));
+    KV_TRY(check_ptr(tile_scale, 4, "tile_scale"));
+    KV_TRY(check_ptr(out, 16, "out"));
+    const int bits = kind == KVARN_KIND_K ? cfg->k_bits : cfg->v_bits;
+    cudaError_t e = kvarn::launch_dequant(bits, (int)kind, codes, params, tile_scale, n_tiles,
+                                          original_basis, !(cfg->flags & KVARN_FLAG_NO_ROTATE), out,
+                                          (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+    return ok();
+}
+
+static kvarn_status check_decode_shape(const kvarn_config* cfg, int B, int Hq, int Hkv, int max_tiles) {
+    KV_TRY(check_cfg(cfg));
+    if (B < 0 || B > 65535) return fail(KVARN_ERR_INVALID_ARG, "B = %d outside 0..65535", B);
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+        return fail(KVARN_ERR_INVALID_ARG, "Hq = %d, Hkv = %d: need Hq a positive multiple of Hkv", Hq, Hkv);
+    const int g = Hq / Hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(KVARN_ERR_UNSUPPORTED, "Hq / Hkv = %d; supported: 1, 2, 4, 8", g);
+    if (Hkv * (g > 4 ? g / 4 : 1) > 65535) return fail(KVARN_ERR_INVALID_ARG, "Hkv = %d too large", Hkv);
+    if (max_tiles < 0 || max_tiles > (1 << 24))
+        return fail(KVARN_ERR_INVALID_ARG, "max_tiles = %d outside 0..2^24", max_tiles);
+    return KVARN_OK;
+}
+
+size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int Hkv, int max_tiles) {
+    if (check_decode_shape(cfg, B, Hq, Hkv, max_tiles) != KVARN_OK) return 0;
+    return kvarn::plan_decode(B, Hq, Hkv, max_tiles).workspace_bytes;
+}
+
+kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
+                                    int Hkv, const void* k_codes, const void* k_params,
+                                    const float* k_scale, const void* v_codes,
+                                    const void* v_params, const float* v_scale,
+                                    const int32_t* block_table, int max_tiles,
+                                    const int32_t* seq_lens, const int32_t* seq_lens_host,
+                                    const void* k_tail_bf16, const void* v_tail_bf16,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    float* out, kvarn_stream_t stream) {
+    KV_TRY(check_decode_shape(cfg, B, Hq, Hkv, max_tiles));
+    if (!isfinite(softmax_scale)) return fail(KVARN_ERR_INVALID_ARG, "softmax_scale is not finite");
+    if (B == 0) return ok();
+    KV_TRY(check_ptr(q_bf16, 16, "q_bf16"));
+    KV_TRY(check_ptr(seq_lens, 4, "seq_lens"));
+    KV_TRY(check_ptr(k_tail_bf16, 16, "k_tail_bf16"));
+    KV_TRY(check_ptr(v_tail_bf16, 16, "v_tail_bf16"));
+    KV_TRY(check_ptr(out, 16, "out"));
+    if (max_tiles > 0) {
+        KV_TRY(check_ptr(k_codes, 16, "k_codes"));
+        KV_TRY(check_ptr(k_params, 16, "k_params"));
+        KV_TRY(check_ptr(k_scale, 4, "k_scale"));
+        KV_TRY(check_ptr(v_codes, 16, "v_codes"));
+        KV_TRY(check_ptr(v_params, 16, "v_params"));
+        KV_TRY(check_ptr(v_scale, 4, "v_scale"));
+        KV_TRY(check_ptr(block_table, 4, "block_table"));
+    }
+    if (seq_lens_host) {
+        const long long cap = (long long)max_tiles * KVARN_TILE_TOKENS + (KVARN_TILE_TOKENS - 1);
+        for (int b = 0; b < B; ++b)
+            if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
+                return fail(KVARN_ERR_INVALID_ARG, "seq_lens[%d] = %d outside 0..%lld", b, seq_lens_host[b], cap);
+    }
+    const kvarn::DecodePlan plan = kvarn::plan_decode(B, Hq, Hkv, max_tiles);
+    KV_TRY(check_ptr(workspace, 16, "workspace"));
+    if (workspace_bytes < plan.workspace_bytes)
+        return fail(KVARN_ERR_WORKSPACE, "workspace_bytes = %zu < required %zu", workspace_bytes,
+                    plan.workspace_bytes);
+    cudaError_t e = kvarn::launch_decode(cfg->k_bits, cfg->v_bits, Hq / Hkv, q_bf16, B, Hq, Hkv, k_codes,
+                                         k_params, k_scale, v_codes, v_params, v_scale, block_table,
+                                         max_tiles, seq_lens, k_tail_bf16, v_tail_bf16, softmax_scale,
+                                         !(cfg->flags & KVARN_FLAG_NO_ROTATE), workspace, plan, out,
+                                         (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    return ok();
+}
+
+kvarn_status kvarn_device_error(uint32_t* code_out) {
+    if (!code_out) return fail(KVARN_ERR_INVALID_ARG, "code_out is NULL");
+    unsigned int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+    e = kvarn::read_and_clear_device_error(&v);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    *code_out = v;
+    return ok();
+}
+
+const char* kvarn_status_string(kvarn_status status) {
+    switch (status) {
+        case KVARN_OK: return "KVARN_OK";
+        case KVARN_ERR_INVALID_ARG: return "KVARN_ERR_INVALID_ARG: an argument is out of range";
+        case KVARN_ERR_UNSUPPORTED: return "KVARN_ERR_UNSUPPORTED: valid but not implemented";
+        case KVARN_ERR_CUDA: return "KVARN_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KVARN_ERR_WORKSPACE: return "KVARN_ERR_WORKSPACE: workspace too small";
+    }
+    return "unknown kvarn_status";
+}
+
+const char* kvarn_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,36 @@
+// Launchers behind the libkvarn C-ABI (host side, not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvarn {
+
+size_t encode_smem_bytes();
+cudaError_t read_and_clear_device_error(unsigned int* out);
+cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
+                          void* params, float* tile_scale, int iters, int rotate, int normalize,
+                          cudaStream_t stream);
+
+cudaError_t launch_dequant(int bits, int kind, const void* codes, const void* params,
+                           const float* tile_scale, int64_t n_tiles, int original_basis,
+                           int rotate, float* out, cudaStream_t stream);
+
+// Split-K plan for decode attention: tiles per split and number of splits.
+struct DecodePlan {
+    int tiles_per_split;
+    int splits;
+    size_t workspace_bytes;
+};
+DecodePlan plan_decode(int B, int Hq, int Hkv, int max_tiles);
+
+cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int B, int Hq, int Hkv,
+                          const void* k_codes, const void* k_params, const float* k_scale,
+                          const void* v_codes, const void* v_params, const float* v_scale,
+                          const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
+                          const void* k_tail, const void* v_tail, float softmax_scale, int rotate,
+                          void* workspace, const DecodePlan& plan, float* out,
+                          cudaStream_t stream);
+
+}  // namespace kvarn

@@ -23,7 +23,9 @@
  *     returns a non-zero kvarn_status, enqueues nothing and leaves every output untouched;
  *     kvarn_last_error() then describes the problem (thread-local text).
  *   - A launch failure returns KVARN_ERR_CUDA (the CUDA error is consumed with cudaGetLastError).
- *   - Head dimension and tile length are fixed at 128. Every pointer must be 16-byte aligned.
+ *   - Head dimension and tile length are fixed at 128.  Tensor pointers (x, codes, params, out,
+ *     q, tails, workspace) must be 16-byte aligned; float/int32 arrays (tile_scale, k_scale,
+ *     v_scale, block_table, seq_lens) 4-byte aligned.
  *
  * Packed tile format (one 128-token x 128-channel tile of one head; all little-endian)
  *   Tile axes: t = token (0..127), j = channel (0..127).  Y = X * H is the rotated tile, where
@@ -155,6 +157,12 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
                                     const void* k_tail_bf16, const void* v_tail_bf16,
                                     float softmax_scale, void* workspace, size_t workspace_bytes,
                                     float* out, kvarn_stream_t stream);
+
+/* Reads and clears the device-side error word of the current device, after synchronising it.
+ * The encoder sets bit 1 (value 1) when a TMA bulk copy does not complete within its bounded
+ * wait; the affected tiles are then left unwritten.  *code_out = 0 means no such event.
+ * (A library diagnostic; the pages have no counterpart.) */
+kvarn_status kvarn_device_error(uint32_t* code_out);
 
 /* Static text for a status code. */
 const char* kvarn_status_string(kvarn_status status);

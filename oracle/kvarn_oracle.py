@@ -175,7 +175,7 @@ def tile_factor(s_max: float, m_max: float) -> float:
 
 
 def encode_tile(x: np.ndarray, kind: str, bits: int, iters: int = DEFAULT_ITERS,
-                rotate: bool = True, normalize: bool = True) -> dict:
+                rotate: bool = True, normalize: bool = True, forced: dict | None = None) -> dict:
     """Encode one 128 x 128 tile (rows = tokens, columns = channels) of K (kind 'K') or V ('V').
 
     Steps, in the order the pages give them ([agihunt] pipeline paragraph; [paperlayer]
@@ -207,7 +207,11 @@ def encode_tile(x: np.ndarray, kind: str, bits: int, iters: int = DEFAULT_ITERS,
          S1 = 0.
     Returns the codes [token, channel] (uint8), the stored parameters (as the values the format
     holds) and the unrounded quantities the parity tests use to recognise rounding ties.
+
+    forced: optional {"s2", "S1", "Z", "g"} values that replace the computed ones from that step
+    on (teacher forcing, so a parity test can compare each later step on identical inputs).
     """
+    forced = forced or {}
     assert kind in ("K", "V") and bits in (2, 4, 8, 16)
     x = np.asarray(x, dtype=np.float64)
     assert x.shape == (TILE, TILE)
@@ -219,6 +223,8 @@ def encode_tile(x: np.ndarray, kind: str, bits: int, iters: int = DEFAULT_ITERS,
     log_other = log_r if kind == "K" else log_c
     s2_raw = np.exp(log_other - log_other.mean())  # geometric mean 1
     s2 = np.clip(e4m3_round(s2_raw), E4M3_MIN_SUBNORMAL, E4M3_MAX)
+    if "s2" in forced:
+        s2 = np.asarray(forced["s2"], dtype=np.float64)
     if kind == "K":
         w = y / s2[:, None]  # token factor divides each row; groups are columns
         wg = w.T  # [group, element]
@@ -230,10 +236,12 @@ def encode_tile(x: np.ndarray, kind: str, bits: int, iters: int = DEFAULT_ITERS,
     mx = wg.max(axis=1)
     scale = (mx - m) / levels
     g = tile_factor(scale.max(), np.abs(m).max())
+    if "g" in forced:
+        g = float(forced["g"])
     s1_raw = scale / g
     z_raw = m / g
-    s1 = e4m3_round_up(s1_raw)
-    z = fp16_round(z_raw)
+    s1 = e4m3_round_up(s1_raw) if "S1" not in forced else np.asarray(forced["S1"], np.float64)
+    z = fp16_round(z_raw) if "Z" not in forced else np.asarray(forced["Z"], np.float64)
     with np.errstate(divide="ignore", invalid="ignore"):
         u = (wg / g - z[:, None]) / s1[:, None]
     u = np.where(s1[:, None] > 0, u, 0.0)

@@ -1,0 +1,130 @@
+"""The C-ABI library builds, loads and exports every call include/kvarn.h declares; host-side
+argument validation returns the documented status without touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvarn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_kv_cache_kvarn_gb300 import _build
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    srcs = [os.path.join(_build.CSRC, s) for s in os.listdir(_build.CSRC)] + [HEADER]
+    if not os.path.exists(_build.LIB) or os.path.getmtime(_build.LIB) < max(map(os.path.getmtime, srcs)):
+        _build.build()
+    return kv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvarn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for want in ("kvarn_encode_blocks", "kvarn_dequant", "kvarn_decode_attention",
+                 "kvarn_decode_workspace_size", "kvarn_config_from_preset"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (kvarn_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_presets_and_sizes(lib):
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    c = kv.kvarn_config_from_preset("kvarn_k4v2_g128")
+    assert (c.k_bits, c.v_bits, c.sinkhorn_iters, c.flags) == (4, 2, 8, 0)
+    c = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    assert (c.k_bits, c.v_bits, c.sinkhorn_iters) == (2, 2, 8)
+    with pytest.raises(kv.KvarnError, match="unknown preset"):
+        kv.kvarn_config_from_preset("kvarn_k3v3")
+    assert kv.kvarn_tile_code_bytes(2) == 4096 and kv.kvarn_tile_code_bytes(4) == 8192
+    assert kv.kvarn_tile_code_bytes(3) == 0 and kv.kvarn_tile_param_bytes() == 512
+    for s in range(5):
+        assert kv.kvarn_status_string(s).startswith("KVARN_")
+
+
+def _cfg(**kw):
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    return kv.make_config(**kw)
+
+
+FAKE = 0x7F0000000000  # a 16-byte aligned address the calls must reject or never touch
+
+
+def test_encode_validation_needs_no_gpu(lib):
+    cfg = _cfg()
+    enc = lib.kvarn_encode_blocks
+    assert enc(None, 0, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(_cfg(k_bits=3)), 0, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(_cfg(sinkhorn_iters=65)), 0, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(_cfg(flags=8)), 0, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(cfg), 2, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(cfg), 0, FAKE, -1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(cfg), 0, None, 1, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(cfg), 0, FAKE + 8, 1, FAKE, FAKE, FAKE, None) == 1
+    assert b"aligned" in lib.kvarn_last_error()
+    assert enc(ctypes.byref(cfg), 0, FAKE, 1, FAKE, FAKE, FAKE + 2, None) == 1
+    assert enc(ctypes.byref(cfg), 0, None, 0, None, None, None, None) == 0  # empty: no-op
+
+
+def test_dequant_validation_needs_no_gpu(lib):
+    cfg = _cfg()
+    dq = lib.kvarn_dequant
+    assert dq(ctypes.byref(cfg), 0, FAKE, FAKE, FAKE, 1, 2, FAKE, None) == 1
+    assert dq(ctypes.byref(cfg), 0, FAKE, FAKE, FAKE, 2 ** 31, 0, FAKE, None) == 1
+    assert dq(ctypes.byref(cfg), 0, FAKE, FAKE, FAKE, 1, 0, FAKE + 4, None) == 1
+    assert dq(ctypes.byref(cfg), 1, None, None, None, 0, 1, None, None) == 0
+
+
+def _decode(lib, cfg, B=2, Hq=8, Hkv=2, max_tiles=4, lens_host=None, ws=FAKE, ws_bytes=1 << 30,
+            scale=0.1, tail=FAKE):
+    host = None
+    if lens_host is not None:
+        arr = (ctypes.c_int32 * len(lens_host))(*lens_host)
+        host = ctypes.cast(arr, ctypes.c_void_p)
+    return lib.kvarn_decode_attention(ctypes.byref(cfg), FAKE, B, Hq, Hkv, FAKE, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, max_tiles, FAKE, host, tail, FAKE,
+                                      ctypes.c_float(scale), ws, ws_bytes, FAKE, None)
+
+
+def test_decode_validation_needs_no_gpu(lib):
+    cfg = _cfg()
+    assert _decode(lib, cfg, Hq=6, Hkv=4) == 1
+    assert _decode(lib, cfg, Hq=12, Hkv=4) == 2  # group 3: unsupported
+    assert _decode(lib, cfg, Hq=32, Hkv=2) == 2  # group 16
+    assert _decode(lib, cfg, B=-1) == 1
+    assert _decode(lib, cfg, max_tiles=-1) == 1
+    assert _decode(lib, cfg, scale=float("inf")) == 1
+    assert _decode(lib, cfg, tail=None) == 1
+    assert _decode(lib, cfg, lens_host=[5, 4 * 128 + 128]) == 1  # over 128*max_tiles + 127
+    assert _decode(lib, cfg, lens_host=[-1, 3]) == 1
+    assert _decode(lib, cfg, ws_bytes=16) == 4
+    assert b"workspace" in lib.kvarn_last_error()
+    assert _decode(lib, cfg, B=0) == 0
+
+
+def test_workspace_plan(lib):
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    cfg = _cfg()
+    # 16 tiles per split; (m, l, 2 pad, o[128]) floats per (sequence, query head, split)
+    assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == 16 * 32 * 16 * 132 * 4
+    assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == 4 * 40 * 64 * 132 * 4
+    assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == 1 * 4 * 1 * 132 * 4
+    assert kv.kvarn_decode_workspace_size(cfg, 1, 6, 4, 1) == 0

@@ -1,0 +1,116 @@
+"""GPU encode / dequant parity with the fp64 oracle, through the C-ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvarn_oracle as o
+from tests._parity import compare_encode, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _encode_gpu(kv, cfg, kind, x_tiles):
+    n = x_tiles.shape[0]
+    bits = cfg.k_bits if kind == kv.KVARN_KIND_K else cfg.v_bits
+    codes = torch.empty(n, 128 * 16 * bits, dtype=torch.uint8, device="cuda")
+    params = torch.empty(n, 512, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(n, dtype=torch.float32, device="cuda")
+    kv.kvarn_encode_blocks(cfg, kind, x_tiles, codes, params, scale)
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_error() == 0
+    return codes, params, scale
+
+
+def _check(kv, cfg, x_tiles, label, rotate=True, normalize=True, kinds=("K", "V")):
+    xs = x_tiles.float().cpu().double().numpy()
+    out = {}
+    for kind, name in ((kv.KVARN_KIND_K, "K"), (kv.KVARN_KIND_V, "V")):
+        if name not in kinds:
+            continue
+        bits = cfg.k_bits if name == "K" else cfg.v_bits
+        codes, params, scale = _encode_gpu(kv, cfg, kind, x_tiles)
+        st = compare_encode(xs, name, bits, codes.cpu().numpy(), params.cpu().numpy(),
+                            scale.cpu().numpy(), cfg.sinkhorn_iters, rotate, normalize)
+        print(label, name, st)
+        out[name] = (codes, params, scale, st)
+    return out
+
+
+def test_config0_tiny_codec(kv):
+    # one kv head, K and V of 1024 tokens (8 tiles each), 2-bit, seed 0
+    k, v = kv.synthetic.outlier_kv(0, 1, 1024)
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    _check(kv, cfg, k.reshape(8, 128, 128).cuda(), "config0")
+    _check(kv, cfg, v.reshape(8, 128, 128).cuda(), "config0")
+
+
+@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+def test_config1_batched_encode_full(kv, preset):
+    # 64 sequences x 8 kv heads x one 128-token block, seed 1: 512 K tiles and 512 V tiles
+    k, v = kv.synthetic.outlier_kv(1, 64 * 8, 128, device="cuda")
+    cfg = kv.kvarn_config_from_preset(preset)
+    res_k = _check(kv, cfg, k.reshape(-1, 128, 128), preset + " K-cache", kinds=("K",))
+    res_v = _check(kv, cfg, v.reshape(-1, 128, 128), preset + " V-cache", kinds=("V",))
+    for st in (res_k["K"][3], res_v["V"][3]):
+        assert st["free_code_mismatch"] <= 1e-4 * st["elements"]
+
+
+def test_edge_tiles(kv):
+    cfg = kv.kvarn_config_from_preset("kvarn_k4v2_g128")
+    base = kv.synthetic.outlier_kv(5, 1, 128)[0].reshape(1, 128, 128)
+    tiles = [torch.zeros(128, 128), torch.full((128, 128), 3.0), base[0].float() * 2.0 ** 40,
+             base[0].float() * 2.0 ** -40, torch.randn(128, 128, generator=torch.Generator().manual_seed(3))]
+    t = torch.zeros(128, 128)
+    t[:, 7] = 5.0  # one non-zero channel
+    tiles.append(t)
+    t = torch.zeros(128, 128)
+    t[9, :] = -2.0  # one non-zero token
+    tiles.append(t)
+    x = torch.stack(tiles).to(torch.bfloat16).cuda()
+    res = _check(kv, cfg, x, "edge")
+    codes, params, scale, _ = res["K"]
+    assert scale[0].item() == 1.0 and not codes[0].any()
+
+
+@pytest.mark.parametrize("flags,iters", [(0, 0), (0, 1), (0, 20), (1, 8), (2, 8), (3, 0)])
+def test_ablation_flags_and_iterations(kv, flags, iters):
+    k, _ = kv.synthetic.outlier_kv(6, 3, 128)
+    cfg = kv.make_config(4, 2, iters, flags)
+    _check(kv, cfg, k.reshape(3, 128, 128).cuda(), f"flags={flags} iters={iters}",
+           rotate=not (flags & 1), normalize=not (flags & 2))
+
+
+def test_persistent_grid_many_tiles_and_empty(kv):
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    k, _ = kv.synthetic.outlier_kv(7, 1, 128 * 333, device="cuda")
+    x = k.reshape(333, 128, 128)
+    codes, params, scale = _encode_gpu(kv, cfg, kv.KVARN_KIND_K, x)
+    # every tile independent of its position in the grid: re-encode a few tiles alone
+    for i in (0, 151, 152, 332):
+        c1, p1, s1 = _encode_gpu(kv, cfg, kv.KVARN_KIND_K, x[i:i + 1].contiguous())
+        assert torch.equal(c1[0], codes[i]) and torch.equal(p1[0], params[i]) and s1[0] == scale[i]
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    kv.kvarn_encode_blocks(cfg, kv.KVARN_KIND_K, torch.empty(0, 128, 128, dtype=torch.bfloat16, device="cuda"),
+                           empty, empty, torch.empty(0, device="cuda"))
+
+
+@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+def test_dequant_matches_oracle_on_identical_packed_input(kv, preset):
+    cfg = kv.kvarn_config_from_preset(preset)
+    k, v = kv.synthetic.outlier_kv(8, 40, 128, device="cuda")
+    for kind, name, x in ((kv.KVARN_KIND_K, "K", k), (kv.KVARN_KIND_V, "V", v)):
+        bits = cfg.k_bits if name == "K" else cfg.v_bits
+        x = x.reshape(-1, 128, 128)
+        codes, params, scale = _encode_gpu(kv, cfg, kind, x)
+        for basis in (0, 1):
+            out = torch.empty(x.shape[0], 128, 128, device="cuda")
+            kv.kvarn_dequant(cfg, kind, codes, params, scale, out, original_basis=basis)
+            torch.cuda.synchronize()
+            ref = o.dequant_blocks(codes.cpu().numpy(), params.cpu().numpy(), scale.cpu().numpy(),
+                                   name, bits, original_basis=bool(basis))
+            got = out.cpu().double().numpy()
+            for t in range(x.shape[0]):
+                rms = np.sqrt(np.mean(ref[t] ** 2))
+                assert np.abs(got[t] - ref[t]).max() <= 1e-3 * rms
+        # reconstruction quality sanity: the codec estimate is close to the input
+        assert rel_l2(got, x.float().cpu().double().numpy()) < (0.5 if bits == 2 else 0.15)

@@ -1,0 +1,147 @@
+"""GPU decode attention over the packed cache vs the fp64 oracle, on identical packed inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvarn_oracle as o
+from tests._parity import rel_l2
+
+pytestmark = pytest.mark.gpu
+DECODE_REL_L2 = 1e-3
+
+
+def build_cache(kv, cfg, B, Hkv, lens, seed, device="cuda"):
+    """Encode every full 128-token block of each (sequence, kv head) with libkvarn into a pool whose
+    tile ids are scattered by a random permutation; tails hold the remaining tokens in bf16."""
+    lens = [int(v) for v in lens]
+    nt = max(1, max(lens) // 128 + 1)
+    U = B * Hkv
+    k, v = kv.synthetic.outlier_kv(seed, U, nt * 128, device=device)
+    kt = k.reshape(U * nt, 128, 128)
+    vt = v.reshape(U * nt, 128, 128)
+    pools = {}
+    for kind, name, x in ((kv.KVARN_KIND_K, "k", kt), (kv.KVARN_KIND_V, "v", vt)):
+        bits = cfg.k_bits if name == "k" else cfg.v_bits
+        codes = torch.empty(U * nt, 128 * 16 * bits, dtype=torch.uint8, device=device)
+        params = torch.empty(U * nt, 512, dtype=torch.uint8, device=device)
+        scale = torch.empty(U * nt, dtype=torch.float32, device=device)
+        kv.kvarn_encode_blocks(cfg, kind, x, codes, params, scale)
+        pools[name] = (codes, params, scale)
+    perm = kv.synthetic.tile_permutation(seed, U * nt, device=device)
+    for name in ("k", "v"):
+        c, p, s = pools[name]
+        c2, p2, s2 = torch.empty_like(c), torch.empty_like(p), torch.empty_like(s)
+        c2[perm], p2[perm], s2[perm] = c, p, s
+        pools[name] = (c2, p2, s2)
+    table = perm.to(torch.int32).reshape(B, Hkv, nt).contiguous()
+    k_tail = torch.zeros(B, Hkv, 128, 128, dtype=torch.bfloat16, device=device)
+    v_tail = torch.zeros_like(k_tail)
+    kr = k.reshape(B, Hkv, nt * 128, 128)
+    vr = v.reshape(B, Hkv, nt * 128, 128)
+    for b, L in enumerate(lens):
+        full, tail = (L // 128) * 128, L % 128
+        k_tail[b, :, :tail] = kr[b, :, full:full + tail]
+        v_tail[b, :, :tail] = vr[b, :, full:full + tail]
+    return dict(pools=pools, table=table, k_tail=k_tail, v_tail=v_tail, nt=nt,
+                seq_lens=torch.tensor(lens, dtype=torch.int32, device=device), lens=lens)
+
+
+def run_gpu(kv, cfg, q, Hkv, c, scale):
+    B, Hq = q.shape[:2]
+    ws = torch.empty(kv.kvarn_decode_workspace_size(cfg, B, Hq, Hkv, c["nt"]) // 4 + 4,
+                     dtype=torch.float32, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    kc, kp, ks = c["pools"]["k"]
+    vc, vp, vs = c["pools"]["v"]
+    kv.kvarn_decode_attention(cfg, q, Hkv, kc, kp, ks, vc, vp, vs, c["table"], c["seq_lens"],
+                              c["k_tail"], c["v_tail"], scale, ws, out, seq_lens_host=c["lens"])
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_out(cfg, q, Hkv, c, scale, pairs=None):
+    kc, kp, ks = (t.cpu().numpy() for t in c["pools"]["k"])
+    vc, vp, vs = (t.cpu().numpy() for t in c["pools"]["v"])
+    rotate = not (cfg.flags & 1)
+    return o.decode_attention(q.float().cpu().double().numpy(), q.shape[1], Hkv, kc, kp, ks, vc, vp,
+                              vs, c["table"].cpu().numpy(), c["lens"], c["k_tail"].float().cpu().numpy(),
+                              c["v_tail"].float().cpu().numpy(), scale, cfg.k_bits, cfg.v_bits,
+                              rotate=rotate, pairs=pairs)
+
+
+def check(gpu, ref, pairs=None):
+    gpu = gpu.cpu().double().numpy()
+    B, Hq = gpu.shape[:2]
+    pairs = pairs or [(b, h) for b in range(B) for h in range(Hq)]
+    worst = 0.0
+    for b, h in pairs:
+        if not np.any(ref[b, h]):
+            assert not np.any(gpu[b, h]), (b, h)
+            continue
+        e = rel_l2(gpu[b, h], ref[b, h])
+        worst = max(worst, e)
+        assert e <= DECODE_REL_L2, f"(b={b}, h={h}) rel-L2 {e:.2e}"
+    return worst
+
+
+@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+def test_small_shapes_lengths_and_tails(kv, preset):
+    cfg = kv.kvarn_config_from_preset(preset)
+    lens = [0, 1, 127, 128, 129, 5 * 128 + 77, 16 * 128, 16 * 128 + 5, 33 * 128 + 100]
+    c = build_cache(kv, cfg, len(lens), 2, lens, seed=11)
+    q = kv.synthetic.queries(11, len(lens), 8, device="cuda")
+    scale = 1 / math.sqrt(128)
+    gpu = run_gpu(kv, cfg, q, 2, c, scale)
+    ref = oracle_out(cfg, q, 2, c, scale)
+    print("worst rel-L2", check(gpu, ref))
+    assert torch.all(gpu[0] == 0)
+
+
+@pytest.mark.parametrize("k_bits,v_bits,hq,hkv", [(2, 2, 3, 3), (4, 4, 4, 2), (2, 4, 16, 2), (4, 2, 8, 1)])
+def test_group_sizes_and_bit_widths(kv, k_bits, v_bits, hq, hkv):
+    cfg = kv.make_config(k_bits, v_bits, 8, 0)
+    lens = [3 * 128 + 9, 20 * 128]
+    c = build_cache(kv, cfg, 2, hkv, lens, seed=12 + hq)
+    q = kv.synthetic.queries(12, 2, hq, device="cuda")
+    gpu = run_gpu(kv, cfg, q, hkv, c, 0.07)
+    check(gpu, oracle_out(cfg, q, hkv, c, 0.07))
+
+
+def test_no_rotate_flag(kv):
+    cfg = kv.make_config(4, 2, 8, 1)
+    lens = [7 * 128 + 3]
+    c = build_cache(kv, cfg, 1, 2, lens, seed=13)
+    q = kv.synthetic.queries(13, 1, 8, device="cuda")
+    gpu = run_gpu(kv, cfg, q, 2, c, 0.09)
+    check(gpu, oracle_out(cfg, q, 2, c, 0.09))
+
+
+def test_config2_full_size_sampled(kv):
+    # Qwen3-4B shaped decode: 32 query / 8 kv heads, batch 16, 32768 tokens, 2-bit cache, seed 2
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    B, Hq, Hkv, L = 16, 32, 8, 32768
+    c = build_cache(kv, cfg, B, Hkv, [L] * B, seed=2)
+    q = kv.synthetic.queries(2, B, Hq, device="cuda")
+    scale = 1 / math.sqrt(128)
+    gpu = run_gpu(kv, cfg, q, Hkv, c, scale)
+    assert torch.isfinite(gpu).all()
+    pairs = [(0, 0), (5, 13), (15, 31)]
+    ref = oracle_out(cfg, q, Hkv, c, scale, pairs=pairs)
+    print("config2 worst rel-L2", check(gpu, ref, pairs))
+
+
+def test_config3_ragged_long_context_sampled(kv):
+    # Phi-4 shaped decode: 40 query / 10 kv heads, batch 4, lengths U[65536, 131072], 4-bit K
+    cfg = kv.kvarn_config_from_preset("kvarn_k4v2_g128")
+    B, Hq, Hkv = 4, 40, 10
+    lens = kv.synthetic.ragged_lengths(3, B, 65536, 131072)
+    c = build_cache(kv, cfg, B, Hkv, lens, seed=3)
+    q = kv.synthetic.queries(3, B, Hq, device="cuda")
+    scale = 1 / math.sqrt(128)
+    gpu = run_gpu(kv, cfg, q, Hkv, c, scale)
+    assert torch.isfinite(gpu).all()
+    pairs = [(0, 1), (3, 39)]
+    ref = oracle_out(cfg, q, Hkv, c, scale, pairs=pairs)
+    print("config3 lens", lens, "worst rel-L2", check(gpu, ref, pairs))
