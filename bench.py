@@ -1,0 +1,398 @@
+"""Benchmark of the KVarN codec hot path on GB300 (libkvarn).
+
+One step = the whole hot path once:
+  * encode of one batch of completed blocks: 64 sequences x 8 kv heads x one 128-token block of
+    bf16 K and V (a Qwen3-4B layer), 2-bit preset (kvarn_k2v2_g128), and
+  * one decode-attention step over a 2-bit packed cache: batch 16, 32 query / 8 kv heads,
+    head_dim 128, 32768 tokens per sequence, one bf16 query per head.
+Inputs are seeded synthetic tensors already resident in HBM; the 302 MB packed cache is larger
+than L2 and L2 is also flushed (a 256 MiB write) before every timed step.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle instead, on a
+bounded sample of the same workload, scaled to the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-encode GB/s + 2-bit decode-attn us/step at 32k ctx; % of HBM peak"
+ENC_SEQ, ENC_HKV = 64, 8
+DEC_B, DEC_HQ, DEC_HKV, DEC_L = 16, 32, 8, 32768
+WORKLOAD = ("encode 64 seq x 8 kv heads x 128-token block (K and V, bf16, 2-bit) + decode attention "
+            "B=16, 32q/8kv heads, d=128, 32768-token 2-bit packed cache")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def enc_bytes(n_tiles_per_kind, k_bits=2, v_bits=2):
+    inp = 2 * n_tiles_per_kind * 128 * 128 * 2
+    out = n_tiles_per_kind * ((128 * 16 * k_bits + 512 + 4) + (128 * 16 * v_bits + 512 + 4))
+    return inp, out
+
+
+def dec_bytes(k_bits=2, v_bits=2):
+    tiles = DEC_B * DEC_HKV * (DEC_L // 128)
+    cache = tiles * ((128 * 16 * k_bits + 512 + 4) + (128 * 16 * v_bits + 512 + 4))
+    q = DEC_B * DEC_HQ * 128 * 2
+    out = DEC_B * DEC_HQ * 128 * 4
+    return cache, q, out
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_kv_cache_kvarn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvarn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# reference arm / cpu baseline: the fp64 oracle on host cores, bounded sample, scaled to us/step
+# ------------------------------------------------------------------------------------------------
+def oracle_step_estimate(budget_s=20.0):
+    import numpy as np
+    import torch
+
+    from bit_kv_cache_kvarn_gb300 import synthetic
+    from oracle import kvarn_oracle as o
+
+    k, v = synthetic.outlier_kv(1, 8, 128)  # 8 units of the encode workload
+    xk = k.reshape(-1, 128, 128).float().double().numpy()
+    xv = v.reshape(-1, 128, 128).float().double().numpy()
+    t0 = time.perf_counter()
+    n_enc = 0
+    while time.perf_counter() - t0 < budget_s * 0.4 and n_enc < 64:
+        o.encode_tile(xk[n_enc % 8], "K", 2)
+        o.encode_tile(xv[n_enc % 8], "V", 2)
+        n_enc += 1
+    t_enc_tile_pair = (time.perf_counter() - t0) / n_enc
+    # decode: one (sequence, kv head) unit over 32768 tokens, dequant + attention for 4 heads
+    n_units = 0
+    t1 = time.perf_counter()
+    kc, kp, ks, _ = o.encode_blocks(xk[:1], "K", 2)
+    vc, vp, vs, _ = o.encode_blocks(xv[:1], "V", 2)
+    nt = DEC_L // 128
+    kc, kp, ks = np.repeat(kc, nt, 0), np.repeat(kp, nt, 0), np.repeat(ks, nt, 0)
+    vc, vp, vs = np.repeat(vc, nt, 0), np.repeat(vp, nt, 0), np.repeat(vs, nt, 0)
+    table = np.arange(nt).reshape(1, 1, nt)
+    tails = np.zeros((1, 1, 128, 128))
+    q = torch.randn(1, 4, 128, generator=torch.Generator().manual_seed(2)).double().numpy()
+    t1 = time.perf_counter()
+    while time.perf_counter() - t1 < budget_s * 0.6 and n_units < 8:
+        o.decode_attention(q, 4, 1, kc, kp, ks, vc, vp, vs, table, [DEC_L], tails, tails,
+                           1 / math.sqrt(128), 2, 2)
+        n_units += 1
+    t_unit = (time.perf_counter() - t1) / n_units
+    n_enc_tiles = ENC_SEQ * ENC_HKV
+    step_s = n_enc_tiles * t_enc_tile_pair + DEC_B * DEC_HKV * t_unit
+    sample = (f"{n_enc} K+V tile encodes and {n_units} (sequence, kv head) decode units of 32768 "
+              f"tokens x 4 heads, scaled to {n_enc_tiles} tile pairs + {DEC_B * DEC_HKV} units")
+    return step_s * 1e6, sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    times = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        us, sample = oracle_step_estimate(budget_s=max(2.0, 60.0 / (args.warmup + args.steps)))
+        if i >= args.warmup:
+            times.append(us)
+    v = statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(v / 1000, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "cache > L2; CPU run"},
+        "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+def build_decode_cache(kv, cfg, device):
+    import torch
+
+    U = DEC_B * DEC_HKV
+    nt = DEC_L // 128
+    k, v = kv.synthetic.outlier_kv(2, U, DEC_L, device=device)
+    pools = {}
+    for kind, name, x in ((kv.KVARN_KIND_K, "k", k), (kv.KVARN_KIND_V, "v", v)):
+        bits = cfg.k_bits if name == "k" else cfg.v_bits
+        codes = torch.empty(U * nt, 128 * 16 * bits, dtype=torch.uint8, device=device)
+        params = torch.empty(U * nt, 512, dtype=torch.uint8, device=device)
+        scale = torch.empty(U * nt, dtype=torch.float32, device=device)
+        kv.kvarn_encode_blocks(cfg, kind, x.reshape(-1, 128, 128), codes, params, scale)
+        pools[name] = (codes, params, scale)
+    del k, v
+    perm = kv.synthetic.tile_permutation(2, U * nt, device=device)
+    for name in ("k", "v"):
+        c, p, s = pools[name]
+        c2, p2, s2 = torch.empty_like(c), torch.empty_like(p), torch.empty_like(s)
+        c2[perm], p2[perm], s2[perm] = c, p, s
+        pools[name] = (c2, p2, s2)
+    table = perm.to(torch.int32).reshape(DEC_B, DEC_HKV, nt).contiguous()
+    tail = torch.zeros(DEC_B, DEC_HKV, 128, 128, dtype=torch.bfloat16, device=device)
+    lens = torch.full((DEC_B,), DEC_L, dtype=torch.int32, device=device)
+    torch.cuda.synchronize()
+    return pools, table, tail, lens
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    kv.load()
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+
+    # encode workload (config: Qwen3-4B layer, 64 seq x 8 kv heads x 128 tokens), seed 1
+    n_enc = ENC_SEQ * ENC_HKV
+    ek, ev = kv.synthetic.outlier_kv(1, n_enc, 128, device=device)
+    ek, ev = ek.reshape(n_enc, 128, 128), ev.reshape(n_enc, 128, 128)
+    out_k = (torch.empty(n_enc, 4096, dtype=torch.uint8, device=device),
+             torch.empty(n_enc, 512, dtype=torch.uint8, device=device),
+             torch.empty(n_enc, dtype=torch.float32, device=device))
+    out_v = tuple(torch.empty_like(t) for t in out_k)
+    # decode workload, seed 2
+    pools, table, tail, lens = build_decode_cache(kv, cfg, device)
+    q = kv.synthetic.queries(2, DEC_B, DEC_HQ, device=device)
+    ws = torch.empty(kv.kvarn_decode_workspace_size(cfg, DEC_B, DEC_HQ, DEC_HKV, DEC_L // 128) // 4,
+                     dtype=torch.float32, device=device)
+    out = torch.empty(DEC_B, DEC_HQ, 128, dtype=torch.float32, device=device)
+    sm_scale = 1 / math.sqrt(128)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def enc():
+        kv.kvarn_encode_blocks(cfg, kv.KVARN_KIND_K, ek, *out_k)
+        kv.kvarn_encode_blocks(cfg, kv.KVARN_KIND_V, ev, *out_v)
+
+    def dec(qq=q, o=out):
+        kv.kvarn_decode_attention(cfg, qq, DEC_HKV, *pools["k"], *pools["v"], table, lens, tail, tail,
+                                  sm_scale, ws, o)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        enc()
+        dec()
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_error() == 0
+
+    ev_ = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    marks = [(ev_(), ev_(), ev_()) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            flush.fill_(float(s))
+            a, b, c = marks[s]
+            a.record()
+            enc()
+            b.record()
+            dec()
+            c.record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    enc_ms = [a.elapsed_time(b) for a, b, _ in marks]
+    dec_ms = [b.elapsed_time(c) for _, b, c in marks]
+    step_ms = statistics.mean(e + d for e, d in zip(enc_ms, dec_ms))
+    t = torch.tensor([step_ms, statistics.mean(enc_ms), statistics.mean(dec_ms)], device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms, enc_ms_m, dec_ms_m = (float(x) for x in t)
+
+    # end to end through host buffers: H2D of the new K/V blocks and queries, D2H of the output
+    hk = ek.cpu().pin_memory()
+    hv = ev.cpu().pin_memory()
+    hq = q.cpu().pin_memory()
+    hout = torch.empty_like(out, device="cpu").pin_memory()
+    dk, dv, dq = torch.empty_like(ek), torch.empty_like(ev), torch.empty_like(q)
+    e2e = []
+    for s in range(args.warmup + args.steps):
+        flush.fill_(float(s))
+        a, c = ev_(), ev_()
+        a.record()
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        kv.kvarn_encode_blocks(cfg, kv.KVARN_KIND_K, dk, *out_k)
+        kv.kvarn_encode_blocks(cfg, kv.KVARN_KIND_V, dv, *out_v)
+        dec(dq, out)
+        hout.copy_(out, non_blocking=True)
+        c.record()
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            e2e.append(a.elapsed_time(c))
+    e2e_ms = statistics.mean(e2e)
+    t = torch.tensor([e2e_ms], device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_ms = float(t[0])
+
+    if rank == 0:
+        hbm, src = peaks()
+        e_in, e_out = enc_bytes(n_enc)
+        d_cache, d_q, d_out = dec_bytes()
+        enc_gbs = (e_in + e_out) / (enc_ms_m * 1e-3) / 1e9
+        enc_in_gbs = e_in / (enc_ms_m * 1e-3) / 1e9
+        dec_alg = d_cache + d_q + d_out
+        dec_gbs = dec_alg / (dec_ms_m * 1e-3) / 1e9
+        traffic = ncu_traffic("kvarn_decode_attention")
+        # N replicas each do one step of work in the max-over-ranks time
+        value_us = step_ms * 1000 / world
+        line = {
+            "metric": METRIC, "value": round(value_us, 2), "unit": "us/step", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "preset": "kvarn_k2v2_g128", "sinkhorn_iters": 8,
+                       "l2": "flushed (256 MiB write) before every step; decode cache 302 MB > L2",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "encode": {"us": round(enc_ms_m * 1000, 2), "gbs_bf16_input": round(enc_in_gbs, 1),
+                       "gbs_read_plus_write": round(enc_gbs, 1), "hbm_frac": round(enc_gbs / hbm, 4),
+                       "bytes_per_step": e_in + e_out, "launches_per_step": 2},
+            "decode": {"us": round(dec_ms_m * 1000, 2),
+                       "tokens_per_s": round(DEC_B / (dec_ms_m * 1e-3), 1),
+                       "kv_tokens_per_s": round(DEC_B * DEC_L / (dec_ms_m * 1e-3), 1),
+                       "gbs": round(dec_gbs, 1), "hbm_frac": round(dec_gbs / hbm, 4),
+                       "bytes_per_step": dec_alg, "launches_per_step": 2},
+            "roofline": {"kernel": "kvarn_decode_attention (split + merge launches)", "bound": "hbm",
+                         "achieved": round(dec_gbs, 1), "peak": hbm, "peak_source": src,
+                         "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
+                         "traffic": traffic},
+            "e2e": {"value": round(e2e_ms * 1000 / world, 2), "unit": "us/step",
+                    "h2d_bytes_per_step": 2 * ek.numel() * 2 + q.numel() * 2,
+                    "d2h_bytes_per_step": out.numel() * 4},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": round(t_wall, 4),
+        }
+        if not args.no_cpu_baseline:
+            us, sample = oracle_step_estimate(budget_s=20.0)
+            line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": 1,
+                                    "kind": "oracle", "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -41,6 +41,7 @@ struct EncodeSmem {
     float grp_scale[kTile];
     float grp_z[kTile];                    // zero-point (value of the FP16 code)
     float grp_inv_s1[kTile];               // 1 / S1 (0 where S1 = 0)
+    float grp_s1[kTile];                   // S1
     float oth_inv_s2[kTile];               // 1 / s2 along the other axis
     float bred[kWarps];                    // block reductions
     float bcast[4];
@@ -394,6 +395,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             reinterpret_cast<__half*>(sm.params + 256)[tid] = zh;
             sm.grp_z[tid] = __half2float(zh);
             sm.grp_inv_s1[tid] = s1 > 0.f ? 1.f / s1 : 0.f;
+            sm.grp_s1[tid] = s1;
         }
         __syncthreads();
 
@@ -405,7 +407,12 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * i) : t;
-                const float u = (yy[k][i].x * inv_g - sm.grp_z[grp]) * sm.grp_inv_s1[grp];
+                const float d = fmaf(yy[k][i].x, inv_g, -sm.grp_z[grp]);
+                float u = d * sm.grp_inv_s1[grp];
+                // Near a half-way point the reciprocal product can break an exact tie the wrong
+                // way; redo it with a correctly rounded division so ties go to even.
+                if (fabsf(u - floorf(u) - 0.5f) < 1e-4f && sm.grp_inv_s1[grp] > 0.f)
+                    u = __fdiv_rn(d, sm.grp_s1[grp]);
                 int c = __float2int_rn(u);
                 c = min(max(c, 0), kLevels);
                 packed |= (uint32_t)c << (BITS * i);
