@@ -205,7 +205,7 @@ def build_decode_cache(kv, cfg, device):
 
     U = DEC_B * DEC_HKV
     nt = DEC_L // 128
-    k, v = kv.synthetic.outlier_kv(2, U, DEC_L, device=device)
+    k, v = kv.synthetic.outlier_kv(2, U, DEC_L, device=device)  # noqa: F841
     pools = {}
     for kind, name, x in ((kv.KVARN_KIND_K, "k", k), (kv.KVARN_KIND_V, "v", v)):
         bits = cfg.k_bits if name == "k" else cfg.v_bits
@@ -229,6 +229,8 @@ def build_decode_cache(kv, cfg, device):
 
 
 def run_gpu(args):
+    global DEC_L
+    DEC_L = args.ctx
     import torch
     import torch.distributed as dist
 
@@ -269,10 +271,15 @@ def run_gpu(args):
         kv.kvarn_decode_attention(cfg, qq, DEC_HKV, *pools["k"], *pools["v"], table, lens, tail, tail,
                                   sm_scale, ws, o)
 
+    torch.cuda.empty_cache()
+    do_enc = args.only in ("all", "encode")
+    do_dec = args.only in ("all", "decode")
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        enc()
-        dec()
+        if do_enc:
+            enc()
+        if do_dec:
+            dec()
     torch.cuda.synchronize()
     assert kv.kvarn_device_error() == 0
 
@@ -287,9 +294,11 @@ def run_gpu(args):
             flush.fill_(float(s))
             a, b, c = marks[s]
             a.record()
-            enc()
+            if do_enc:
+                enc()
             b.record()
-            dec()
+            if do_dec:
+                dec()
             c.record()
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -310,7 +319,7 @@ def run_gpu(args):
     hout = torch.empty_like(out, device="cpu").pin_memory()
     dk, dv, dq = torch.empty_like(ek), torch.empty_like(ev), torch.empty_like(q)
     e2e = []
-    for s in range(args.warmup + args.steps):
+    for s in range(0 if args.no_e2e else args.warmup + args.steps):
         flush.fill_(float(s))
         a, c = ev_(), ev_()
         a.record()
@@ -325,7 +334,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if s >= args.warmup:
             e2e.append(a.elapsed_time(c))
-    e2e_ms = statistics.mean(e2e)
+    e2e_ms = statistics.mean(e2e) if e2e else float("nan")
     t = torch.tensor([e2e_ms], device=device)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -365,7 +374,7 @@ def run_gpu(args):
             "e2e": {"value": round(e2e_ms * 1000 / world, 2), "unit": "us/step",
                     "h2d_bytes_per_step": 2 * ek.numel() * 2 + q.numel() * 2,
                     "d2h_bytes_per_step": out.numel() * 4},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": (2 * do_enc + 2 * do_dec) * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed_region": round(t_wall, 4),
         }
@@ -385,6 +394,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ctx", type=int, default=32768, help="decode context (profiling runs only)")
+    ap.add_argument("--only", default="all", choices=["all", "encode", "decode"],
+                    help="time one part (profiling runs only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
