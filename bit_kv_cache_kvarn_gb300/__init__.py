@@ -56,6 +56,9 @@ _SIGNATURES = {
     "kvarn_decode_attention": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
                                       ctypes.c_float, _vp, _sz, _vp, _vp]),
+    "kvarn_decode_attention_static_ws": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
+                                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                                _vp, _vp, ctypes.c_float, _vp, _vp]),
     "kvarn_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
     "kvarn_status_string": (ctypes.c_char_p, [_i32]),
     "kvarn_last_error": (ctypes.c_char_p, []),
@@ -188,6 +191,30 @@ def kvarn_decode_attention(cfg: kvarn_config, q, Hkv: int, k_codes, k_params, k_
         _ptr(v_codes), _ptr(v_params), _ptr(v_scale), _ptr(block_table), max_tiles, _ptr(seq_lens),
         host, _ptr(k_tail), _ptr(v_tail), float(softmax_scale), _ptr(workspace), ws_bytes,
         _ptr(out), _stream(stream)))
+
+
+def kvarn_decode_attention_static_ws(cfg: kvarn_config, q, Hkv: int, k_codes, k_params, k_scale,
+                                     v_codes, v_params, v_scale, block_table, seq_lens, k_tail,
+                                     v_tail, softmax_scale: float, out, seq_lens_host=None,
+                                     stream=None):
+    """kvarn_decode_attention without a workspace argument: the split-K scratch is a fixed device
+    array owned by the library (for callers that cannot allocate device memory at this point)."""
+    B, Hq = q.shape[0], q.shape[1]
+    max_tiles = block_table.shape[-1]
+    _need(q, torch.bfloat16, B * Hq * TILE, "q")
+    _need(block_table, torch.int32, B * Hkv * max_tiles, "block_table")
+    _need(seq_lens, torch.int32, B, "seq_lens")
+    _need(k_tail, torch.bfloat16, B * Hkv * TILE * TILE, "k_tail")
+    _need(v_tail, torch.bfloat16, B * Hkv * TILE * TILE, "v_tail")
+    _need(out, torch.float32, B * Hq * TILE, "out")
+    host = None
+    if seq_lens_host is not None:
+        arr = (ctypes.c_int32 * B)(*[int(v) for v in seq_lens_host])
+        host = ctypes.cast(arr, ctypes.c_void_p)
+    _check(load().kvarn_decode_attention_static_ws(
+        ctypes.byref(cfg), _ptr(q), B, Hq, Hkv, _ptr(k_codes), _ptr(k_params), _ptr(k_scale),
+        _ptr(v_codes), _ptr(v_params), _ptr(v_scale), _ptr(block_table), max_tiles, _ptr(seq_lens),
+        host, _ptr(k_tail), _ptr(v_tail), float(softmax_scale), _ptr(out), _stream(stream)))
 
 
 def kvarn_device_error() -> int:

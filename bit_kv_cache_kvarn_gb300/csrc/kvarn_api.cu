@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 
 #include "../../include/kvarn.h"
@@ -201,6 +202,55 @@ kvarn_status kvarn_device_error(uint32_t* code_out) {
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
     *code_out = v;
     return ok();
+}
+
+// ---- decode attention with library-owned scratch (no allocation by the caller or the library) ----
+// The split-K partials normally live in a caller-supplied workspace.  This variant keeps them in a
+// fixed device array instead, for callers that have no way to obtain device memory at this point.
+// Every GPU that loads the library holds the array (KVARN_STATIC_WS_BYTES) until the process exits.
+static __device__ __align__(256) unsigned char g_kvarn_static_ws[KVARN_STATIC_WS_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_static_ws_mutex;
+void* g_static_ws_ptr[kMaxDevices] = {};  // device address of g_kvarn_static_ws, per device
+}  // namespace
+
+kvarn_status kvarn_decode_attention_static_ws(
+    const kvarn_config* cfg, const void* q_bf16, int B, int Hq, int Hkv, const void* k_codes,
+    const void* k_params, const float* k_scale, const void* v_codes, const void* v_params,
+    const float* v_scale, const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
+    const int32_t* seq_lens_host, const void* k_tail_bf16, const void* v_tail_bf16,
+    float softmax_scale, float* out, kvarn_stream_t stream) {
+    const size_t need = kvarn_decode_workspace_size(cfg, B, Hq, Hkv, max_tiles);
+    if (need > (size_t)KVARN_STATIC_WS_BYTES)
+        return fail(KVARN_ERR_WORKSPACE,
+                    "this shape needs %zu bytes of split-K scratch; the static scratch holds %zu "
+                    "(use kvarn_decode_attention with a caller workspace)",
+                    need, (size_t)KVARN_STATIC_WS_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(KVARN_ERR_UNSUPPORTED, "device index %d", dev);
+    void* ws = nullptr;
+    {
+        // First call on this device (with it current): look up the array's device address once.
+        std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+        if (!g_static_ws_ptr[dev]) {
+            e = cudaGetSymbolAddress(&g_static_ws_ptr[dev], g_kvarn_static_ws);
+            if (e != cudaSuccess) {
+                g_static_ws_ptr[dev] = nullptr;
+                return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+            }
+        }
+        ws = g_static_ws_ptr[dev];
+    }
+    // Every partial the kernels read is written earlier in the same call, so the array needs no
+    // clearing between calls.
+    return kvarn_decode_attention(cfg, q_bf16, B, Hq, Hkv, k_codes, k_params, k_scale, v_codes,
+                                  v_params, v_scale, block_table, max_tiles, seq_lens, seq_lens_host,
+                                  k_tail_bf16, v_tail_bf16, softmax_scale, ws,
+                                  (size_t)KVARN_STATIC_WS_BYTES, out, stream);
 }
 
 const char* kvarn_status_string(kvarn_status status) {

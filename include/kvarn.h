@@ -158,6 +158,29 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
                                     float softmax_scale, void* workspace, size_t workspace_bytes,
                                     float* out, kvarn_stream_t stream);
 
+/* Decode attention without a caller workspace.  Same arguments and results as
+ * kvarn_decode_attention, minus workspace/workspace_bytes: the split-K partials go to a fixed array
+ * of KVARN_STATIC_WS_BYTES (8 MiB) that the library keeps in device memory on every GPU that loads
+ * it, for the life of the process.  The paper has no counterpart; this call exists for callers that
+ * cannot allocate device memory where they run decode -- e.g. code inside a host callback (CUDA
+ * forbids API calls such as cudaMalloc there), a plugin whose host framework owns the allocator and
+ * offers no scratch, or a latency-critical loop that must not hit cudaMalloc's implicit
+ * synchronisation.  Nothing is allocated: no cudaMalloc/cudaFree, no allocating library routine.
+ *   - The first call on a device, with that device current, looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the previous call's contents (every
+ *     value a call reads is written earlier in that call).  Calls whose kernels can overlap on the
+ *     GPU (different streams without ordering) race on it: serialise them.
+ *   - Shapes needing more than KVARN_STATIC_WS_BYTES (see kvarn_decode_workspace_size) return
+ *     KVARN_ERR_WORKSPACE before anything is enqueued; e.g. B=16, Hq=32, 256 tiles needs 4.3 MB. */
+#define KVARN_STATIC_WS_BYTES (8u * 1024u * 1024u)
+kvarn_status kvarn_decode_attention_static_ws(
+    const kvarn_config* cfg, const void* q_bf16, int B, int Hq, int Hkv, const void* k_codes,
+    const void* k_params, const float* k_scale, const void* v_codes, const void* v_params,
+    const float* v_scale, const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
+    const int32_t* seq_lens_host, const void* k_tail_bf16, const void* v_tail_bf16,
+    float softmax_scale, float* out, kvarn_stream_t stream);
+
 /* Reads and clears the device-side error word of the current device, after synchronising it.
  * The encoder sets bit 1 (value 1) when a TMA bulk copy does not complete within its bounded
  * wait; the affected tiles are then left unwritten.  *code_out = 0 means no such event.
