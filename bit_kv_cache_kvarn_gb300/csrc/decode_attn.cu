@@ -20,13 +20,16 @@
 
 #include "kvarn_common.cuh"
 #include "kvarn_internal.h"
+#include "tcgen05.cuh"
 
 namespace kvarn {
+
+// Set when a tensor-core completion wait gives up (bounded); read by kvarn_device_error.
+__device__ unsigned int g_decode_error = 0;
 
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = 8;
 constexpr int kTilesPerSplit = 16;
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
 
@@ -56,34 +59,170 @@ __device__ __forceinline__ int clamp_len(int len, int max_tiles) {
     return len < 0 ? 0 : (len > cap ? cap : len);
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int c) {
-    return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+// ---- tensor-core split kernel -------------------------------------------------------------------
+// Per warpgroup and tile: thread r unpacks K row r (token r) to fp16 straight into TMEM (the A
+// operand), builds column r of q'' = q' o S1 (channel r) as fp16 hi/lo pieces in shared memory
+// (the B operand), and one thread issues D_S[128 tok x 16] = A x B.  Thread r then owns token r's
+// scores, runs the online softmax, writes p o S1 for token r as the next B operand, unpacks V row r
+// (channel r) into TMEM and D_O[128 ch x 16] = A x B gives channel r of the output.  N = 16 holds
+// up to 8 heads x (hi, lo).
+
+constexpr int kWG = 2;                    // warpgroups per CTA
+constexpr int kTmemColsPerWG = 128;       // A: 0..63, D_S: 64..79, D_O: 96..111
+constexpr uint32_t kBBytes = 16 * 128 * 2;  // one B operand: 16 rows x 128 K fp16
+constexpr uint32_t kLbo = 128, kSbo = 2048;  // K-major core-matrix strides of B
+constexpr float kWScale = 32.f;          // p * S1 <= 256 -> x32 stays inside fp16
+
+// Byte offset of B element (row n, K index kk) in the K-major no-swizzle layout.
+__device__ __forceinline__ uint32_t b_off(int n, int kk) {
+    return (uint32_t)((kk >> 3) * kLbo + (n >> 3) * kSbo + (n & 7) * 16 + (kk & 7) * 2);
+}
+
+// Position of column c (0..127) of a packed row in the MMA K order, and the power-of-two factor
+// the unpacked code carries there (the B element is multiplied by its inverse).
+template <int BITS>
+__device__ __forceinline__ void k_slot(int c, int& kk, float& inv_pre) {
+    const int h = c & 15, i = c >> 4;
+    if (BITS == 2) {
+        // word h>>1 holds lanes (h even: low half, h odd: high half); pair i -> TMEM column 8w+i
+        const int col = 8 * (h >> 1) + i;
+        kk = 2 * col + (h & 1);
+        inv_pre = ldexpf(1.f, -2 * (i <= 4 ? i : i - 5));
+    } else {
+        // word h holds codes i at bits 4i; pair (i, i+4) -> TMEM column 4h + (i&3)
+        const int ii = i & 3;
+        kk = 2 * (4 * h + ii) + (i >> 2);
+        inv_pre = ldexpf(1.f, -4 * (ii <= 1 ? ii : ii - 2));
+    }
+}
+
+__device__ __forceinline__ uint32_t hsub1024(uint32_t u) {
+    __half2 v = *reinterpret_cast<__half2*>(&u);
+    v = __hsub2(v, __floats2half2_rn(1024.f, 1024.f));
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Unpack one packed row (BITS*4 words) into 64 fp16x2 TMEM columns starting at taddr.
+template <int BITS>
+__device__ __forceinline__ void unpack_row_to_tmem(const uint4 (&row)[BITS], uint32_t taddr) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&row[0]);
+#pragma unroll
+    for (int chunk = 0; chunk < 4; ++chunk) {
+        uint32_t r[16];
+        if (BITS == 2) {
+#pragma unroll
+            for (int ww = 0; ww < 2; ++ww) {
+                const uint32_t x = w[2 * chunk + ww];
+                const uint32_t xs = x >> 10;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t u = (i <= 4) ? ((x & (0x00030003u << (2 * i))) | 0x64006400u)
+                                                : ((xs & (0x00030003u << (2 * (i - 5)))) | 0x64006400u);
+                    r[8 * ww + i] = hsub1024(u);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ww = 0; ww < 4; ++ww) {
+                const uint32_t x = w[4 * chunk + ww];
+                const uint32_t xs = x >> 8;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t u = (i <= 1) ? ((x & (0x000F000Fu << (4 * i))) | 0x64006400u)
+                                                : ((xs & (0x000F000Fu << (4 * (i - 2)))) | 0x64006400u);
+                    r[4 * ww + i] = hsub1024(u);
+                }
+            }
+        }
+        tc::st16(taddr + 16 * chunk, r);
+    }
+}
+
+__device__ __forceinline__ void split_hi_lo(float x, __half& hi, __half& lo) {
+    hi = __float2half_rn(x);
+    lo = __float2half_rn(x - __half2float(hi));
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Barrier over n threads that also returns the AND of every thread's flag.
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool flag) {
+    uint32_t out;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n bar.red.and.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(out)
+        : "r"(id), "r"(n), "r"((uint32_t)flag)
+        : "memory");
+    return out != 0;
+}
+
+template <int KB, int VB>
+struct TileRegs {
+    uint4 k[KB];
+    uint4 v[VB];
+    float s1k, zk, s2k, s1v, zv, s2v, gk, gv;
+};
+
+template <int KB, int VB>
+__device__ __forceinline__ void load_tile(TileRegs<KB, VB>& t, const DecodeArgs& a, int64_t tile, int r) {
+    const uint4* kc = reinterpret_cast<const uint4*>(a.k_codes + tile * (kTile * 16 * KB) + r * (16 * KB));
+    const uint4* vc = reinterpret_cast<const uint4*>(a.v_codes + tile * (kTile * 16 * VB) + r * (16 * VB));
+#pragma unroll
+    for (int u = 0; u < KB; ++u) t.k[u] = __ldg(kc + u);
+#pragma unroll
+    for (int u = 0; u < VB; ++u) t.v[u] = __ldg(vc + u);
+    const uint8_t* kp = a.k_params + tile * KVARN_PARAM_BYTES;
+    const uint8_t* vp = a.v_params + tile * KVARN_PARAM_BYTES;
+    t.s1k = e4m3_value(kp[r]);         // K group scale: channel r
+    t.s2k = e4m3_value(kp[128 + r]);   // K other-axis scale: token r
+    t.zk = fp16_value(reinterpret_cast<const uint16_t*>(kp + 256)[r]);
+    t.s1v = e4m3_value(vp[r]);         // V group scale: token r
+    t.s2v = e4m3_value(vp[128 + r]);   // V other-axis scale: channel r
+    t.zv = fp16_value(reinterpret_cast<const uint16_t*>(vp + 256)[r]);
+    t.gk = a.k_scale[tile];
+    t.gv = a.v_scale[tile];
 }
 
 template <int KB, int VB, int GH>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 decode_split_kernel(DecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t dsm[];
-    float* qr = reinterpret_cast<float*>(dsm);                         // [GH][128]
-    float2* q2_all = reinterpret_cast<float2*>(qr + GH * kTile);       // [warp][64 pairs][GH]
-    float2* wb_all = q2_all + kWarps * 64 * GH;                        // [warp][128 tok][GH]
-    float* ms = reinterpret_cast<float*>(wb_all + kWarps * kTile * GH); // [warp][GH]
-    float* ls = ms + kWarps * GH;                                      // [warp][GH]
-    float* os = ls + kWarps * GH;                                      // [warp][GH][128]
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    uint8_t* b_all = dsm;                                                  // [WG][2][kBBytes]
+    float* qrs = reinterpret_cast<float*>(dsm + kWG * 2 * kBBytes);        // [GH][128] scaled q'
+    float* einv = qrs + GH * kTile;                                        // [GH] 2^-E_h
+    float* red = einv + 8;                                                 // [WG][3][4 warps][8]
+    float* ms = red + kWG * 3 * 4 * 8;                                     // [WG][GH]
+    float* ls = ms + kWG * GH;                                             // [WG][GH]
+    float* os = ls + kWG * GH;                                             // [WG][GH][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(os + kWG * GH * kTile);   // [WG]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kWG);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wg = warp >> 2, wq = warp & 3, r = tid & 127;
     const int split = blockIdx.x;
     const int hblocks = a.group / GH;
     const int kvh = blockIdx.y / hblocks;
-    const int hq0 = kvh * a.group + (blockIdx.y % hblocks) * GH;  // first query head of the CTA
+    const int hq0 = kvh * a.group + (blockIdx.y % hblocks) * GH;
     const int b = blockIdx.z;
-
     const int len = clamp_len(a.seq_lens[b], a.max_tiles);
     const int n_full = len >> 7;
     const int t_begin = split * kTilesPerSplit;
     const int t_end = min(t_begin + kTilesPerSplit, n_full);
 
-    // rotated, scaled queries
+    if (t_begin >= t_end) {  // nothing to read: empty partials
+        for (int e = tid; e < GH * kTile; e += kThreads) {
+            float* dst = a.ws + (((size_t)b * a.Hq + hq0 + (e >> 7)) * a.splits + split) * kWsStride;
+            dst[4 + (e & 127)] = 0.f;
+            if ((e & 127) == 0) {
+                dst[0] = -INFINITY;
+                dst[1] = 0.f;
+            }
+        }
+        return;
+    }
+
+    // rotated queries, scaled so that |q'| * 2^E_h <= 2^6 (then q'' = q' S1 <= 2^14 fits fp16)
     if (warp < GH) {
         const __nv_bfloat16* qp = a.q + ((size_t)b * a.Hq + hq0 + warp) * kTile + 4 * lane;
         const uint2 raw = *reinterpret_cast<const uint2*>(qp);
@@ -95,237 +234,192 @@ decode_split_kernel(DecodeArgs a) {
             fwht128_warp(v, lane);
             sc *= kInvSqrt128;
         }
+        float mx = 0.f;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) qr[warp * kTile + 4 * lane + m] = v[m] * sc;
+        for (int m = 0; m < 4; ++m) {
+            v[m] *= sc;
+            mx = fmaxf(mx, fabsf(v[m]));
+        }
+        mx = warp_max(mx);
+        const int e = mx > 0.f ? 6 - ceil_log2(mx) : 0;
+        const float s = ldexpf(1.f, e);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) qrs[warp * kTile + 4 * lane + m] = v[m] * s;
+        if (lane == 0) einv[warp] = ldexpf(1.f, -e);
     }
+    // B operands: rows 2*GH..15 stay zero
+    for (int i = tid; i < (int)(kWG * 2 * kBBytes / 16); i += kThreads)
+        reinterpret_cast<uint4*>(b_all)[i] = make_uint4(0, 0, 0, 0);
+    if (tid < kWG) mbar_init(&bars[tid], 1);
+    if (warp == 0) tc::alloc(tmem_slot, kWG * kTmemColsPerWG);
+    fence_mbar_init();
+    tc::fence_before();
     __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    float2* q2 = q2_all + warp * 64 * GH;
-    float2* wb = wb_all + warp * kTile * GH;
-    const int lw = lane & 15, ts = lane >> 4;
+    uint8_t* bk = b_all + wg * 2 * kBBytes;
+    uint8_t* bv = bk + kBBytes;
+    float* cpart = red + wg * 96;   // [4 warps][8]
+    float* mpart = cpart + 32;
+    float* zpart = mpart + 32;
+    const uint32_t col0 = tmem + wg * kTmemColsPerWG;
+    const uint32_t lane_addr = col0 + ((uint32_t)(32 * wq) << 16);  // this thread's TMEM lane
+    const uint32_t bk_addr = smem_addr(bk), bv_addr = smem_addr(bv);
+    constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, 16);
+    const int bar_id = 1 + wg;
 
-    float m_run[GH], l_lane[GH];
-    float2 o2[GH][4];
+    // this thread's slot in the MMA K order: as channel r of a K row, and as token r of a V row
+    int kk_k, kk_v;
+    float pre_k, pre_v;
+    k_slot<KB>(r, kk_k, pre_k);
+    k_slot<VB>(r, kk_v, pre_v);
+
+    float m_run[GH], l_part[GH], o[GH];
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
         m_run[h] = -INFINITY;
-        l_lane[h] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o2[h][i] = make_float2(0.f, 0.f);
+        l_part[h] = 0.f;
+        o[h] = 0.f;
     }
-
+    uint32_t phase = 0;
+    bool alive = true;
     const int32_t* table = a.block_table + ((size_t)b * a.Hkv + kvh) * a.max_tiles;
-    for (int ti = t_begin + warp; ti < t_end; ti += kWarps) {
-        const int64_t tile = table[ti];
-        const uint8_t* kp = a.k_params + tile * KVARN_PARAM_BYTES;
-        const uint8_t* vp = a.v_params + tile * KVARN_PARAM_BYTES;
-        const float gk = a.k_scale[tile];
-        const float gv = a.v_scale[tile];
-        const uint8_t* kc = a.k_codes + tile * (kTile * 16 * KB);
-        const uint8_t* vc = a.v_codes + tile * (kTile * 16 * VB);
 
-        // issue the K code loads first (rows l, l+32, l+64, l+96; 16-byte loads)
-        constexpr int kRowU4 = KB;  // uint4 per row: 2 (2-bit), 4 (4-bit)
-        uint4 rows[4][kRowU4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int u = 0; u < kRowU4; ++u)
-                rows[m][u] = __ldg(reinterpret_cast<const uint4*>(kc + (lane + 32 * m) * (16 * KB)) + u);
+    TileRegs<KB, VB> cur, nxt;
+    int ti = t_begin + wg;
+    if (ti < t_end) load_tile(cur, a, table[ti], r);
+    for (; ti < t_end && alive; ti += kWG) {
+        if (ti + kWG < t_end) load_tile(nxt, a, table[ti + kWG], r);
 
-        // per-tile query factors: q''_j = q'_j S1_j g 2^-shift(j), paired as the codes are
-        float cpart[GH];
-#pragma unroll
-        for (int h = 0; h < GH; ++h) cpart[h] = 0.f;
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-            const int p = lane + 32 * pp;
-            int ja, jb;
-            float pre;
-            if (KB == 2) {
-                const int w = p >> 3, i = p & 7;
-                ja = 2 * w + 16 * i;
-                jb = ja + 1;
-                pre = ldexpf(1.f, -2 * i);
-            } else {
-                const int w = p >> 2, i = p & 3;
-                ja = w + 16 * i;
-                jb = ja + 64;
-                pre = ldexpf(1.f, -4 * i);
-            }
-            const float sa = e4m3_value(kp[ja]) * gk, sb = e4m3_value(kp[jb]) * gk;
-            const float za = fp16_value(reinterpret_cast<const uint16_t*>(kp + 256)[ja]) * gk;
-            const float zb = fp16_value(reinterpret_cast<const uint16_t*>(kp + 256)[jb]) * gk;
+        // ---- scores: A = K codes (row r = token r), B = q'' pieces (column r = channel r) ----
+        unpack_row_to_tmem<KB>(cur.k, lane_addr);
+        {
+            const float s1 = cur.s1k * pre_k;
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
-                const float qa = qr[h * kTile + ja], qb = qr[h * kTile + jb];
-                q2[p * GH + h] = make_float2(qa * sa * pre, qb * sb * pre);
-                cpart[h] = fmaf(qa, za, fmaf(qb, zb, cpart[h]));
+                __half hi, lo;
+                split_hi_lo(qrs[h * kTile + r] * s1, hi, lo);
+                *reinterpret_cast<__half*>(bk + b_off(2 * h, kk_k)) = hi;
+                *reinterpret_cast<__half*>(bk + b_off(2 * h + 1, kk_k)) = lo;
+                const float c = warp_sum(qrs[h * kTile + r] * cur.zk);
+                if (lane == 0) cpart[wq * 8 + h] = c;
             }
         }
-        float cz_k[GH];
+        fence_proxy_async();
+        tc::wait_st();
+        tc::fence_before();
+        named_sync(bar_id, 128);
+        if (r == 0) {
+            tc::fence_after();
 #pragma unroll
-        for (int h = 0; h < GH; ++h) cz_k[h] = warp_sum(cpart[h]);
-        __syncwarp();
+            for (int s = 0; s < 8; ++s)
+                tc::mma_f16_ts(col0 + 64, col0 + 8 * s, tc::smem_desc(bk_addr + s * 2 * kLbo, kLbo, kSbo), kIdesc, s > 0);
+            tc::commit(&bars[wg]);
+        }
+        alive = mbar_wait(&bars[wg], phase, &g_decode_error);
+        phase ^= 1;
+        tc::fence_after();
+        uint32_t d[16];
+        tc::ld16(lane_addr + 64, d);
+        tc::wait_ld();
 
-        // ---- scores for tokens lane + 32 m ----
-        float2 acc[4][GH];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int h = 0; h < GH; ++h) acc[m][h] = make_float2(0.f, 0.f);
-        const float2 neg_magic = make_float2(-kMagic, -kMagic);
-#pragma unroll
-        for (int w = 0; w < 4 * KB; ++w) {
-            uint32_t x[4], xh[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                x[m] = word_of(rows[m][w >> 2], w & 3);
-                xh[m] = x[m] >> 16;
-            }
-            constexpr int kPairs = (KB == 2) ? 8 : 4;
-#pragma unroll
-            for (int i = 0; i < kPairs; ++i) {
-                const uint32_t mask = (KB == 2) ? (3u << (2 * i)) : (15u << (4 * i));
-                const int p = w * kPairs + i;
-                float2 qv[GH];
-#pragma unroll
-                for (int h = 0; h < GH; ++h) qv[h] = q2[p * GH + h];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float2 f = fadd2(make_float2(magic_code(x[m], mask), magic_code(xh[m], mask)), neg_magic);
-#pragma unroll
-                    for (int h = 0; h < GH; ++h) acc[m][h] = ffma2(f, qv[h], acc[m][h]);
-                }
-            }
-        }
-        float s[4][GH];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float s2 = e4m3_value(kp[128 + lane + 32 * m]);
-#pragma unroll
-            for (int h = 0; h < GH; ++h) s[m][h] = (acc[m][h].x + acc[m][h].y + cz_k[h]) * s2;
-        }
-
-        // ---- online softmax (log2 domain), per head ----
-        float alpha[GH], czv[GH];
+        // ---- online softmax over this tile's 128 tokens (thread r = token r), log2 domain ----
+        float s[GH];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
-            float mx = fmaxf(fmaxf(s[0][h], s[1][h]), fmaxf(s[2][h], s[3][h]));
-            mx = warp_max(mx);
-            const float m_new = fmaxf(m_run[h], mx);
+            const float c = cpart[h] + cpart[8 + h] + cpart[16 + h] + cpart[24 + h];
+            s[h] = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1]) + c) * (einv[h] * cur.gk * cur.s2k);
+            const float mx = warp_max(s[h]);
+            if (lane == 0) mpart[wq * 8 + h] = mx;
+        }
+        named_sync(bar_id, 128);
+        float alpha[GH];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            const float mt = fmaxf(fmaxf(mpart[h], mpart[8 + h]), fmaxf(mpart[16 + h], mpart[24 + h]));
+            const float m_new = fmaxf(m_run[h], mt);
             alpha[h] = exp2f(m_run[h] - m_new);
             m_run[h] = m_new;
-            float psum = 0.f, zsum = 0.f;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int t = lane + 32 * m;
-                const float p = exp2f(s[m][h] - m_new);
-                psum += p;
-                zsum = fmaf(p, fp16_value(reinterpret_cast<const uint16_t*>(vp + 256)[t]), zsum);
-                const float w = p * e4m3_value(vp[t]);
-                wb[t * GH + h] = make_float2(w, w);
-            }
-            l_lane[h] = fmaf(l_lane[h], alpha[h], psum);
-            czv[h] = warp_sum(zsum);
+            const float p = exp2f(s[h] - m_new);
+            l_part[h] = fmaf(l_part[h], alpha[h], p);
+            __half hi, lo;
+            split_hi_lo(p * cur.s1v * (kWScale * pre_v), hi, lo);
+            *reinterpret_cast<__half*>(bv + b_off(2 * h, kk_v)) = hi;
+            *reinterpret_cast<__half*>(bv + b_off(2 * h + 1, kk_v)) = lo;
+            const float z = warp_sum(p * cur.zv);
+            if (lane == 0) zpart[wq * 8 + h] = z;
         }
-        __syncwarp();
 
-        // ---- V: lane (lw, ts) accumulates channels lw + 16 i over tokens ts + 2 n ----
-        float2 a2[GH][4];
+        // ---- PV: A = V codes (row r = channel r), B = p S1 pieces (column r = token r) ----
+        unpack_row_to_tmem<VB>(cur.v, lane_addr);
+        fence_proxy_async();
+        tc::wait_st();
+        tc::fence_before();
+        named_sync(bar_id, 128);
+        if (r == 0) {
+            tc::fence_after();
 #pragma unroll
-        for (int h = 0; h < GH; ++h)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a2[h][i] = make_float2(0.f, 0.f);
-#pragma unroll 4
-        for (int n0 = 0; n0 < 64; n0 += 8) {
-            uint32_t xv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = ts + 2 * (n0 + u);
-                xv[u] = (VB == 2) ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(vc + t * 32) + lw)
-                                  : __ldg(reinterpret_cast<const uint32_t*>(vc + t * 64) + lw);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = ts + 2 * (n0 + u);
-                float2 wv[GH];
-#pragma unroll
-                for (int h = 0; h < GH; ++h) wv[h] = wb[t * GH + h];
-                const uint32_t xhi = xv[u] >> 16;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float2 f;
-                    if (VB == 2)
-                        f = make_float2(magic_code(xv[u], 3u << (2 * i)), magic_code(xv[u], 3u << (2 * i + 8)));
-                    else
-                        f = make_float2(magic_code(xv[u], 15u << (4 * i)), magic_code(xhi, 15u << (4 * i)));
-                    f = fadd2(f, neg_magic);
-#pragma unroll
-                    for (int h = 0; h < GH; ++h) a2[h][i] = ffma2(f, wv[h], a2[h][i]);
-                }
-            }
+            for (int s2 = 0; s2 < 8; ++s2)
+                tc::mma_f16_ts(col0 + 96, col0 + 8 * s2, tc::smem_desc(bv_addr + s2 * 2 * kLbo, kLbo, kSbo), kIdesc, s2 > 0);
+            tc::commit(&bars[wg]);
         }
-        // fold 2^-shift, the zero-point term (once per channel: ts == 0 lanes) and g * s2_j
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int ja = lw + 16 * i, jb = ja + 64;
-            const float2 sc = make_float2(gv * e4m3_value(vp[128 + ja]), gv * e4m3_value(vp[128 + jb]));
-            const float2 pre = (VB == 2) ? make_float2(ldexpf(1.f, -2 * i), ldexpf(1.f, -2 * i - 8))
-                                         : make_float2(ldexpf(1.f, -4 * i), ldexpf(1.f, -4 * i));
+        alive = mbar_wait(&bars[wg], phase, &g_decode_error) && alive;
+        phase ^= 1;
+        tc::fence_after();
+        tc::ld16(lane_addr + 96, d);
+        tc::wait_ld();
+        {
+            const float sc = cur.gv * cur.s2v;  // channel r
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
-                const float cz = ts == 0 ? czv[h] : 0.f;
-                const float2 v = ffma2(a2[h][i], pre, make_float2(cz, cz));
-                o2[h][i] = ffma2(o2[h][i], make_float2(alpha[h], alpha[h]), fmul2(v, sc));
+                const float z = zpart[h] + zpart[8 + h] + zpart[16 + h] + zpart[24 + h];
+                const float acc = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) * (1.f / kWScale) + z;
+                o[h] = fmaf(o[h], alpha[h], acc * sc);
             }
         }
-        __syncwarp();  // q2 / wb are rewritten by the next tile
+        cur = nxt;
+        // the scratch (cpart/mpart/zpart, B) of this tile is reused by the next: all threads must
+        // be past their reads; the barrier also makes the give-up decision uniform
+        tc::fence_before();
+        alive = named_sync_and(bar_id, 128, alive);
+        tc::fence_after();
     }
 
-    // ---- merge the 8 warps of this CTA ----
+    // ---- merge the warpgroups of this CTA ----
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
-        const float lw_sum = warp_sum(l_lane[h]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            o2[h][i].x += __shfl_xor_sync(0xffffffffu, o2[h][i].x, 16);
-            o2[h][i].y += __shfl_xor_sync(0xffffffffu, o2[h][i].y, 16);
-        }
-        if (ts == 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                os[(warp * GH + h) * kTile + lw + 16 * i] = o2[h][i].x;
-                os[(warp * GH + h) * kTile + lw + 16 * i + 64] = o2[h][i].y;
-            }
-        }
-        if (lane == 0) {
-            ms[warp * GH + h] = m_run[h];
-            ls[warp * GH + h] = lw_sum;
-        }
+        const float lsum = warp_sum(l_part[h]);
+        if (lane == 0) red[wg * 96 + wq * 8 + h] = lsum;
+        os[(wg * GH + h) * kTile + r] = o[h];
+        if (r == 0) ms[wg * GH + h] = m_run[h];
     }
+    tc::fence_before();
     __syncthreads();
     for (int e = tid; e < GH * kTile; e += kThreads) {
         const int h = e >> 7, j = e & 127;
         float mmax = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, ms[w * GH + h]);
-        float o = 0.f, l = 0.f;
+        for (int g = 0; g < kWG; ++g) mmax = fmaxf(mmax, ms[g * GH + h]);
+        float ov = 0.f, l = 0.f;
         if (mmax != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = exp2f(ms[w * GH + h] - mmax);
-                o = fmaf(os[(w * GH + h) * kTile + j], f, o);
-                l = fmaf(ls[w * GH + h], f, l);
+            for (int g = 0; g < kWG; ++g) {
+                const float f = exp2f(ms[g * GH + h] - mmax);
+                const float lg = red[g * 96 + h] + red[g * 96 + 8 + h] + red[g * 96 + 16 + h] + red[g * 96 + 24 + h];
+                ov = fmaf(os[(g * GH + h) * kTile + j], f, ov);
+                l = fmaf(lg, f, l);
             }
         }
         float* dst = a.ws + (((size_t)b * a.Hq + hq0 + h) * a.splits + split) * kWsStride;
-        dst[4 + j] = o;
+        dst[4 + j] = ov;
         if (j == 0) {
             dst[0] = mmax;
             dst[1] = l;
         }
     }
+    tc::fence_after();
+    if (warp == 0) tc::dealloc(tmem, kWG * kTmemColsPerWG);
 }
 
 // One warp per (sequence, query head): merge splits, inverse rotation, bf16 tail, normalise.
@@ -387,8 +481,10 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
 
 template <int GH>
 size_t split_smem_bytes() {
-    return (size_t)GH * kTile * 4 + (size_t)kWarps * 64 * GH * 8 + (size_t)kWarps * kTile * GH * 8 +
-           (size_t)kWarps * GH * 8 + (size_t)kWarps * GH * kTile * 4;
+    size_t bytes = (size_t)kWG * 2 * kBBytes + (size_t)GH * kTile * 4 + 8 * 4 + kWG * 3 * 4 * 8 * 4 +
+                   2 * kWG * GH * 4 + (size_t)kWG * GH * kTile * 4 + kWG * 8 + 16;
+    // at least 80 KB, so no more than two CTAs (2 x 256 TMEM columns) share an SM
+    return bytes < 80 * 1024 ? 80 * 1024 : bytes;
 }
 
 template <int KB, int VB, int GH>
@@ -405,7 +501,8 @@ template <int KB, int VB>
 cudaError_t run_split_g(const DecodeArgs& a, int gh, dim3 grid, cudaStream_t stream) {
     if (gh == 1) return run_split<KB, VB, 1>(a, grid, stream);
     if (gh == 2) return run_split<KB, VB, 2>(a, grid, stream);
-    return run_split<KB, VB, 4>(a, grid, stream);
+    if (gh == 4) return run_split<KB, VB, 4>(a, grid, stream);
+    return run_split<KB, VB, 8>(a, grid, stream);
 }
 
 }  // namespace
@@ -416,6 +513,15 @@ DecodePlan plan_decode(int B, int Hq, int /*Hkv*/, int max_tiles) {
     p.splits = max_tiles <= 0 ? 1 : (max_tiles + kTilesPerSplit - 1) / kTilesPerSplit;
     p.workspace_bytes = (size_t)B * Hq * p.splits * kWsStride * sizeof(float);
     return p;
+}
+
+cudaError_t read_and_clear_decode_error(unsigned int* out) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(zero));
+    *out = v;
+    return e;
 }
 
 cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int B, int Hq, int Hkv,
@@ -446,7 +552,7 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.splits = plan.splits;
     a.ws = static_cast<float*>(workspace);
     a.out = out;
-    const int gh = group >= 4 ? 4 : group;
+    const int gh = group;  // up to 8 heads x (hi, lo) fill the 16 MMA columns
     dim3 grid(plan.splits, Hkv * (group / gh), B);
     cudaError_t e;
     if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, grid, stream);

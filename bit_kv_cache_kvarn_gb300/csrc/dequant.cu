@@ -42,16 +42,30 @@ dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ pa
     __syncthreads();
 
     const uint8_t* c = codes + tile * kCodeBytes;
+    // K rows are tokens (lane h of row t: channels h + 16 i); V rows are channels (lane tg of
+    // row j: tokens tg + 16 k).  Thread (tg, h) owns tokens tg + 16 k and channels h + 16 i.
+    uint32_t vlanes[8];
+    if (KIND == KVARN_KIND_V) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int j = h + 16 * i;
+            vlanes[i] = (BITS == 2) ? reinterpret_cast<const uint16_t*>(c)[j * 16 + tg]
+                                    : reinterpret_cast<const uint32_t*>(c)[j * 16 + tg];
+        }
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int t = tg + 16 * k;
-        const uint32_t lanev = (BITS == 2) ? reinterpret_cast<const uint16_t*>(c)[t * 16 + h]
-                                           : reinterpret_cast<const uint32_t*>(c)[t * 16 + h];
+        uint32_t lanev = 0;
+        if (KIND == KVARN_KIND_K)
+            lanev = (BITS == 2) ? reinterpret_cast<const uint16_t*>(c)[t * 16 + h]
+                                : reinterpret_cast<const uint32_t*>(c)[t * 16 + h];
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int j = h + 16 * i;
-            const float code = (float)((lanev >> (BITS * i)) & kMask);
+            const uint32_t bits = (KIND == KVARN_KIND_K) ? (lanev >> (BITS * i)) : (vlanes[i] >> (BITS * k));
+            const float code = (float)(bits & kMask);
             const int grp = (KIND == KVARN_KIND_K) ? j : t;
             const int oth = (KIND == KVARN_KIND_K) ? t : j;
             v[i] = s2v[oth] * fmaf(s1v[grp], code, zv[grp]);
@@ -69,14 +83,22 @@ dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ pa
         const int t = idx >> 3, cc = idx & 7;
         float v[16];
         const float* src = ys + t * kYStride + 16 * cc;
+        {
+            // read the 16-byte chunks in a lane-dependent rotation (bank-conflict free), then undo it
+            const int rot = (cc >> 1) & 3;
+            float4 a0 = *reinterpret_cast<const float4*>(src + 4 * ((0 + rot) & 3));
+            float4 a1 = *reinterpret_cast<const float4*>(src + 4 * ((1 + rot) & 3));
+            float4 a2 = *reinterpret_cast<const float4*>(src + 4 * ((2 + rot) & 3));
+            float4 a3 = *reinterpret_cast<const float4*>(src + 4 * ((3 + rot) & 3));
+            rotl4(a0, a1, a2, a3, (4 - rot) & 3);
+            const float4 f[4] = {a0, a1, a2, a3};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int qq = (q + (cc >> 1)) & 3;
-            float4 f = *reinterpret_cast<const float4*>(src + 4 * qq);
-            v[4 * qq] = f.x;
-            v[4 * qq + 1] = f.y;
-            v[4 * qq + 2] = f.z;
-            v[4 * qq + 3] = f.w;
+            for (int q = 0; q < 4; ++q) {
+                v[4 * q] = f[q].x;
+                v[4 * q + 1] = f[q].y;
+                v[4 * q + 2] = f[q].z;
+                v[4 * q + 3] = f[q].w;
+            }
         }
         if (original_basis && rotate) {
             fwht_regs<16>(v);

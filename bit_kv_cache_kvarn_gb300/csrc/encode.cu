@@ -122,25 +122,36 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             const int idx = tid + kThreads * it;
             const int t = idx >> 3, c = idx & 7;
             float v[16];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int half = hh ^ ((c >> 2) & 1);  // bank-conflict-free order
-                uint4 raw = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * half);
-                const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            {
+                // the two 16-byte halves are read in a lane-dependent order (bank-conflict free)
+                const int sw = (c >> 2) & 1;
+                const uint4 ra = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * sw);
+                const uint4 rb = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * (sw ^ 1));
+                const uint4 r0 = sw ? rb : ra, r1 = sw ? ra : rb;
+                const __nv_bfloat162* p0 = reinterpret_cast<const __nv_bfloat162*>(&r0);
+                const __nv_bfloat162* p1 = reinterpret_cast<const __nv_bfloat162*>(&r1);
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    float2 f = __bfloat1622float2(p2[m]);
-                    v[8 * half + 2 * m] = f.x;
-                    v[8 * half + 2 * m + 1] = f.y;
+                    const float2 f0 = __bfloat1622float2(p0[m]);
+                    const float2 f1 = __bfloat1622float2(p1[m]);
+                    v[2 * m] = f0.x;
+                    v[2 * m + 1] = f0.y;
+                    v[8 + 2 * m] = f1.x;
+                    v[8 + 2 * m + 1] = f1.y;
                 }
             }
             if (rotate) fwht_regs<16>(v);
             float* dst = sm.ys + t * kYStride + 16 * c;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int qq = (q + (c >> 1)) & 3;
-                *reinterpret_cast<float4*>(dst + 4 * qq) =
-                    make_float4(v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
+            {
+                // 16-byte chunks stored in a lane-dependent rotation (bank-conflict free)
+                const int rot = (c >> 1) & 3;
+                float4 a0 = make_float4(v[0], v[1], v[2], v[3]), a1 = make_float4(v[4], v[5], v[6], v[7]);
+                float4 a2 = make_float4(v[8], v[9], v[10], v[11]), a3 = make_float4(v[12], v[13], v[14], v[15]);
+                rotl4(a0, a1, a2, a3, rot);
+                *reinterpret_cast<float4*>(dst + 4 * ((0 + rot) & 3)) = a0;
+                *reinterpret_cast<float4*>(dst + 4 * ((1 + rot) & 3)) = a1;
+                *reinterpret_cast<float4*>(dst + 4 * ((2 + rot) & 3)) = a2;
+                *reinterpret_cast<float4*>(dst + 4 * ((3 + rot) & 3)) = a3;
             }
         }
         __syncthreads();
@@ -399,11 +410,15 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         }
         __syncthreads();
 
-        // ---- codes and packing: lane h of token row t holds channels h + 16 i at bits BITS*i ----
+        // ---- codes and packing ----
+        // K rows are tokens: lane h of row t holds channels h + 16 i at bits BITS*i.
+        // V rows are channels: lane tg of row j holds tokens tg + 16 k at bits BITS*k.
+        uint32_t packed[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) packed[q] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int t = tg + 16 * k;
-            uint32_t packed = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * i) : t;
@@ -415,12 +430,20 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                     u = __fdiv_rn(d, sm.grp_s1[grp]);
                 int c = __float2int_rn(u);
                 c = min(max(c, 0), kLevels);
-                packed |= (uint32_t)c << (BITS * i);
+                if (KIND == KVARN_KIND_K)
+                    packed[k] |= (uint32_t)c << (BITS * i);
+                else
+                    packed[i] |= (uint32_t)c << (BITS * k);
             }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int row = (KIND == KVARN_KIND_K) ? (tg + 16 * q) : (h + 16 * q);
+            const int lane16 = (KIND == KVARN_KIND_K) ? h : tg;
             if (BITS == 2)
-                reinterpret_cast<uint16_t*>(sm.codes)[t * 16 + h] = (uint16_t)packed;
+                reinterpret_cast<uint16_t*>(sm.codes)[row * 16 + lane16] = (uint16_t)packed[q];
             else
-                sm.codes[t * 16 + h] = packed;
+                sm.codes[row * 16 + lane16] = packed[q];
         }
         __syncthreads();
 

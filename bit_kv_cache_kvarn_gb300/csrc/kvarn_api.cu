@@ -200,7 +200,10 @@ kvarn_status kvarn_device_error(uint32_t* code_out) {
     if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
     e = kvarn::read_and_clear_device_error(&v);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
-    *code_out = v;
+    unsigned int w = 0;
+    e = kvarn::read_and_clear_decode_error(&w);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    *code_out = v | (w << 1);
     return ok();
 }
 

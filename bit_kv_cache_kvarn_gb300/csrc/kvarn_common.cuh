@@ -131,6 +131,26 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
     }
 }
 
+// Rotate four float4 chunks left by rot (0..3) without dynamic register indexing:
+// afterwards a[q] holds the chunk that was at (q + rot) & 3.
+__device__ __forceinline__ void rotl4(float4& a0, float4& a1, float4& a2, float4& a3, int rot) {
+    if (rot & 1) {
+        float4 t = a0;
+        a0 = a1;
+        a1 = a2;
+        a2 = a3;
+        a3 = t;
+    }
+    if (rot & 2) {
+        float4 t = a0;
+        a0 = a2;
+        a2 = t;
+        t = a1;
+        a1 = a3;
+        a3 = t;
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) v += __shfl_xor_sync(0xffffffffu, v, s);

@@ -9,6 +9,7 @@ namespace kvarn {
 
 size_t encode_smem_bytes();
 cudaError_t read_and_clear_device_error(unsigned int* out);
+cudaError_t read_and_clear_decode_error(unsigned int* out);
 cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
                           cudaStream_t stream);

@@ -34,10 +34,11 @@
  *   Groups of 128 elements follow KIVI [paperlayer, "2 Preliminaries"]: for K a group is one
  *   channel (its 128 tokens); for V a group is one token (its 128 channels).  The "other axis"
  *   is the remaining one (K: token, V: channel).
- *   codes : 16*b bytes per token row (b = bits), rows in token order.  The row is cut into 16
- *           little-endian lanes of b bytes; the code of channel j = 16*i + h (h = j mod 16,
- *           i = j div 16) sits in lane h at bits [b*i, b*i + b).
- *           2-bit tile: 4096 bytes; 4-bit tile: 8192 bytes.
+ *   codes : 128 rows of 16*b bytes (b = bits).  K tiles: row = token, column = channel.  V tiles
+ *           are stored transposed: row = channel, column = token (so decode can stream one
+ *           channel's tokens as one row).  Each row is cut into 16 little-endian lanes of b bytes;
+ *           the code of column c = 16*i + h (h = c mod 16, i = c div 16) sits in lane h at bits
+ *           [b*i, b*i + b).  2-bit tile: 4096 bytes; 4-bit tile: 8192 bytes.
  *   params: 512 bytes per tile:
  *           [  0,128) S1[g]  FP8 E4M3 group scale, indexed by group
  *           [128,256) s2[o]  FP8 E4M3 other-axis scale, indexed by the other axis

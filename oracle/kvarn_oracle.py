@@ -281,10 +281,11 @@ def dequant_tile(codes: np.ndarray, s1, s2, z, g: float, kind: str,
 # Byte layout of a packed tile (the library's format; the pages fix only the accounting)
 # ----------------------------------------------------------------------------------------------
 def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
-    """[128, 128] codes -> [128 * 16 * bits] bytes.
+    """[128 rows, 128 columns] codes -> [128 * 16 * bits] bytes.
 
-    Each token row is 16 little-endian lanes of `bits` bytes; the code of channel j = 16 i + h
-    goes to lane h at bit offset bits * i.
+    Each row is 16 little-endian lanes of `bits` bytes; the code of column j = 16 i + h goes to
+    lane h at bit offset bits * i.  (K tiles are packed with rows = tokens, V tiles with rows =
+    channels; see pack_tile.)
     """
     assert bits in (2, 4)
     codes = np.asarray(codes, dtype=np.uint64)
@@ -334,6 +335,18 @@ def bits_per_element(bits: int) -> float:
     return bits + (8 + 8 + 16) / 128 + 32 / (TILE * TILE)
 
 
+def pack_tile(codes: np.ndarray, bits: int, kind: str) -> np.ndarray:
+    """Packed bytes of one tile's codes [token, channel]: K rows are tokens; V rows are channels
+    (the V tile is stored transposed, so a row holds one channel's 128 tokens)."""
+    return pack_codes(codes if kind == "K" else np.asarray(codes).T, bits)
+
+
+def unpack_tile(packed: np.ndarray, bits: int, kind: str) -> np.ndarray:
+    """Inverse of pack_tile: codes [token, channel]."""
+    c = unpack_codes(packed, bits)
+    return c if kind == "K" else c.T.copy()
+
+
 def encode_blocks(x_tiles: np.ndarray, kind: str, bits: int, iters: int = DEFAULT_ITERS,
                   rotate: bool = True, normalize: bool = True):
     """Encode [n, 128, 128] tiles; returns (codes [n, 16*bits*128] bytes, params [n, 512],
@@ -347,7 +360,7 @@ def encode_blocks(x_tiles: np.ndarray, kind: str, bits: int, iters: int = DEFAUL
     infos = []
     for k in range(n):
         e = encode_tile(x_tiles[k], kind, bits, iters, rotate, normalize)
-        codes[k] = pack_codes(e["codes"], bits)
+        codes[k] = pack_tile(e["codes"], bits, kind)
         params[k] = pack_params(e["S1"], e["s2"], e["Z"])
         scale[k] = e["g"]
         infos.append(e)
@@ -360,7 +373,7 @@ def dequant_blocks(codes: np.ndarray, params: np.ndarray, tile_scale: np.ndarray
     n = codes.shape[0]
     out = np.zeros((n, TILE, TILE))
     for k in range(n):
-        c = unpack_codes(codes[k], bits)
+        c = unpack_tile(codes[k], bits, kind)
         s1, s2, z = unpack_params(params[k])
         out[k] = dequant_tile(c, s1, s2, z, float(tile_scale[k]), kind, original_basis, rotate)
     return out

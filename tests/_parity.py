@@ -51,7 +51,7 @@ def compare_encode(x_tiles, kind, bits, gpu_codes, gpu_params, gpu_scale, iters=
                  code_ties=0, free_code_mismatch=0)
     for k in range(n):
         gs1, gs2, gz = o.unpack_params(gpu_params[k])
-        gcodes = o.unpack_codes(gpu_codes[k], bits)
+        gcodes = o.unpack_tile(gpu_codes[k], bits, kind)
         gg = float(gpu_scale[k])
         free = o.encode_tile(x_tiles[k], kind, bits, iters, rotate, normalize)
         stats["free_code_mismatch"] += int((free["codes"] != gcodes).sum())

@@ -257,10 +257,17 @@ def test_pack_layout_by_hand():
     assert p2[0, 2] == 0b1100 and p2[0].sum() == 0b1100 and p2[1, 0] == 1
     p4 = o.pack_codes(codes, 4).reshape(128, 64)
     assert p4[0, 4] == 0x30 and p4[0].sum() == 0x30 and p4[1, 0] == 1
+    # V tiles are stored transposed: token 17 of channel 0 sits in row 0, lane 1, offset 2
+    v = np.zeros((128, 128), dtype=np.uint8)
+    v[17, 0] = 3
+    pv = o.pack_tile(v, 2, "V").reshape(128, 32)
+    assert pv[0, 2] == 0b1100 and pv.sum() == 0b1100
     rng = np.random.default_rng(14)
     for bits in (2, 4):
         c = rng.integers(0, 2 ** bits, (128, 128)).astype(np.uint8)
         assert np.array_equal(o.unpack_codes(o.pack_codes(c, bits), bits), c)
+        for kind in ("K", "V"):
+            assert np.array_equal(o.unpack_tile(o.pack_tile(c, bits, kind), bits, kind), c)
 
 
 def test_bit_accounting_against_printed_figures():
