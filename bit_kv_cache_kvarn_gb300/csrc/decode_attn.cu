@@ -1,21 +1,31 @@
 // Decode attention over the packed KVarN cache: one query per sequence, grouped-query heads.
 //
 // Method: the quantised cache is restored at attention read time (dimensionstp.github.io review,
-// "4-2 Training strategy"); the query is rotated by the same head-wise Hadamard after RoPE, so
-// keys stay in the rotated basis (paperlayer.ai summary, "A Hadamard Transform Arrangement");
-// the second scale s2 costs one multiply per element and is fused into the dequantisation
-// (paperlayer.ai, "3 Methods" and "I KVarN Dequantization Overhead").  Here both scales are
-// folded out of the inner loops entirely:
-//   K (groups = channels): s_t = s2_t * g * (sum_j q'_j S1_j code_tj + sum_j q'_j Z_j)
-//   V (groups = tokens):   o_j += g * s2_j * (sum_t p_t S1_t code_tj + sum_t p_t Z_t)
+// "4-2 Training strategy"); the query is rotated by the same head-wise Hadamard after RoPE, so keys
+// stay in the rotated basis (paperlayer.ai summary, "A Hadamard Transform Arrangement"); the
+// second scale s2 is fused into the dequantisation (paperlayer.ai, "3 Methods" and "I KVarN
+// Dequantization Overhead").  Here both scales are folded out of the inner products:
+//   K (groups = channels): s_t = s2_t g (sum_j q'_j S1_j code_tj + sum_j q'_j Z_j)
+//   V (groups = tokens):   o_j += g s2_j (sum_t p_t S1_t code_tj + sum_t p_t Z_t)
 //
-// Kernel 1 (split): CTA = (split of the context, kv head, sequence); each of its 8 warps owns whole
-// tiles and keeps its own online-softmax state.  Codes become floats without int->float
-// conversions: OR-ing a code field into the mantissa of 2^23 and subtracting 2^23 gives
-// code * 2^shift exactly, and the 2^-shift is folded into the per-channel factors; pairs of
-// channels then go through packed FFMA2.  Kernel 2 (merge): one warp per query head merges the
-// splits by log-sum-exp, applies the inverse rotation, attends to the unquantised bf16 tail and
-// normalises.  No device-side waits anywhere.
+// Split kernel (5th-generation tensor cores).  The context of each (sequence, kv head) is cut into
+// items of 16 tiles; a CTA holds two warpgroup "workers", each processing a contiguous run of
+// items persistently.  Per tile, one thread of the worker brings the packed K/V codes and
+// parameters into a shared-memory ring with 1-D TMA bulk copies (mbarrier-tracked); then thread r
+// of the worker:
+//   * masks K row r (token r) into fp16 subnormals (code * 2^shift * 2^-24, exact; no conversion)
+//     and stores them in TMEM as the MMA's A operand;
+//   * writes q'' = q' S1 2^-shift for channel r as fp16 hi/lo pieces into the B operand (shared
+//     memory, N-contiguous) -- up to 8 heads x 2 pieces = N 16 -- and its share of sum_j q'_j Z_j;
+//   * after 8 tcgen05.mma (two independent accumulation chains), owns token r's scores, runs the
+//     online softmax (log2 domain), writes p S1 for token r as the next B and its share of
+//     sum_t p_t Z_t, masks V row r (channel r) into A, and after 8 more MMAs owns channel r of
+//     sum_t p_t v_t.
+// The number and depth of MMA instructions, not their FLOPs, set the tensor-core cost here (a
+// dependent K=16 step costs ~200 cycles; N up to 64 costs nothing extra), hence the zero-point
+// sums on the CUDA cores and the two chains.
+// Merge kernel: one warp per (sequence, query head) merges the items by log-sum-exp, applies the
+// inverse rotation, attends to the unquantised bf16 tail and normalises.
 #include <math.h>
 
 #include "kvarn_common.cuh"
@@ -24,14 +34,20 @@
 
 namespace kvarn {
 
-// Set when a tensor-core completion wait gives up (bounded); read by kvarn_device_error.
+// Set when a bounded wait (TMA data or tensor-core completion) gives up; read by kvarn_device_error.
 __device__ unsigned int g_decode_error = 0;
 
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWorkers = 2;                 // warpgroups per CTA
 constexpr int kTilesPerSplit = 16;
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
+constexpr uint32_t kTmemCols = 256;         // worker w: A (64), D_S (2 x 16), D_O (2 x 16) at 128 w
+constexpr uint32_t kBBytes = 256 * 16 * 2;  // one B operand: K = 256 x N = 16 fp16, N-contiguous
+constexpr uint32_t kBKStride = 256, kBNStride = 128;  // core-matrix strides of B along K and N
+constexpr float kWScale = 32.f;             // p S1 <= 256 -> x32 stays inside fp16
+constexpr float kTwo24 = 16777216.f;
 
 struct DecodeArgs {
     const __nv_bfloat16* q;
@@ -59,88 +75,191 @@ __device__ __forceinline__ int clamp_len(int len, int max_tiles) {
     return len < 0 ? 0 : (len > cap ? cap : len);
 }
 
-// ---- tensor-core split kernel -------------------------------------------------------------------
-// Per warpgroup and tile: thread r unpacks K row r (token r) to fp16 straight into TMEM (the A
-// operand), builds column r of q'' = q' o S1 (channel r) as fp16 hi/lo pieces in shared memory
-// (the B operand), and one thread issues D_S[128 tok x 16] = A x B.  Thread r then owns token r's
-// scores, runs the online softmax, writes p o S1 for token r as the next B operand, unpacks V row r
-// (channel r) into TMEM and D_O[128 ch x 16] = A x B gives channel r of the output.  N = 16 holds
-// up to 8 heads x (hi, lo).
+// Shared-memory ring stage: K codes | V codes | K params | V params | g_K, g_V.
+template <int KB, int VB>
+struct Stage {
+    static constexpr uint32_t kK = 0;
+    static constexpr uint32_t kV = KB * 2048;
+    static constexpr uint32_t kKP = kV + VB * 2048;
+    static constexpr uint32_t kVP = kKP + 512;
+    static constexpr uint32_t kG = kVP + 512;
+    static constexpr uint32_t kBytes = kG + 16;
+    static constexpr uint32_t kTx = kG;  // bytes delivered by the bulk copies
+    static constexpr int kCount = (KB + VB == 4) ? 3 : 2;
+};
 
-constexpr int kWG = 2;                    // warpgroups per CTA
-constexpr int kTmemColsPerWG = 128;       // A: 0..63, D_S: 64..79, D_O: 96..111
-constexpr uint32_t kBBytes = 16 * 128 * 2;  // one B operand: 16 rows x 128 K fp16
-constexpr uint32_t kLbo = 128, kSbo = 2048;  // K-major core-matrix strides of B
-constexpr float kWScale = 32.f;          // p * S1 <= 256 -> x32 stays inside fp16
-
-// Byte offset of B element (row n, K index kk) in the K-major no-swizzle layout.
-__device__ __forceinline__ uint32_t b_off(int n, int kk) {
-    return (uint32_t)((kk >> 3) * kLbo + (n >> 3) * kSbo + (n & 7) * 16 + (kk & 7) * 2);
+// Byte offset of the 8 consecutive B elements (rows n0..n0+7) at K index kk.
+__device__ __forceinline__ uint32_t b_off(int n0, int kk) {
+    return (uint32_t)((kk >> 3) * kBKStride + (n0 >> 3) * kBNStride + (kk & 7) * 16);
 }
 
-// Position of column c (0..127) of a packed row in the MMA K order, and the power-of-two factor
-// the unpacked code carries there (the B element is multiplied by its inverse).
+// Position of column c (0..127) of a packed row in the MMA K order, and the power of two
+// (2^-shift) the B element carries to cancel the code's 2^shift.
 template <int BITS>
 __device__ __forceinline__ void k_slot(int c, int& kk, float& inv_pre) {
     const int h = c & 15, i = c >> 4;
     if (BITS == 2) {
-        // word h>>1 holds lanes (h even: low half, h odd: high half); pair i -> TMEM column 8w+i
-        const int col = 8 * (h >> 1) + i;
-        kk = 2 * col + (h & 1);
+        // code i of lane h -> TMEM column 8 i + (h >> 1), half h & 1: the K order is the column order
+        kk = c;
         inv_pre = ldexpf(1.f, -2 * (i <= 4 ? i : i - 5));
     } else {
-        // word h holds codes i at bits 4i; pair (i, i+4) -> TMEM column 4h + (i&3)
+        // codes (ii, ii + 4) of lane h -> TMEM column 16 ii + h, halves 0 / 1
         const int ii = i & 3;
-        kk = 2 * (4 * h + ii) + (i >> 2);
+        kk = 2 * (16 * ii + h) + (i >> 2);
         inv_pre = ldexpf(1.f, -4 * (ii <= 1 ? ii : ii - 2));
     }
 }
 
-__device__ __forceinline__ uint32_t hsub1024(uint32_t u) {
-    __half2 v = *reinterpret_cast<__half2*>(&u);
-    v = __hsub2(v, __floats2half2_rn(1024.f, 1024.f));
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Unpack one packed row (BITS*4 words) into 64 fp16x2 TMEM columns starting at taddr.
+// Mask one packed row (BITS*4 words) into 64 fp16x2 TMEM columns, in the order k_slot describes.
+// A code field left in place is the fp16 subnormal code * 2^shift * 2^-24 (exact).
 template <int BITS>
-__device__ __forceinline__ void unpack_row_to_tmem(const uint4 (&row)[BITS], uint32_t taddr) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&row[0]);
+__device__ __forceinline__ void unpack_row_to_tmem(const uint32_t (&x)[4 * BITS], uint32_t taddr) {
+    constexpr int kWords = 4 * BITS;
+    constexpr int kSh = BITS == 2 ? 10 : 8;
+    uint32_t xs[kWords];
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) xs[w] = x[w] >> kSh;
 #pragma unroll
     for (int chunk = 0; chunk < 4; ++chunk) {
         uint32_t r[16];
         if (BITS == 2) {
 #pragma unroll
-            for (int ww = 0; ww < 2; ++ww) {
-                const uint32_t x = w[2 * chunk + ww];
-                const uint32_t xs = x >> 10;
+            for (int ii = 0; ii < 2; ++ii) {
+                const int i = 2 * chunk + ii;
+                const uint32_t mask = i <= 4 ? (0x00030003u << (2 * i)) : (0x00030003u << (2 * (i - 5)));
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t u = (i <= 4) ? ((x & (0x00030003u << (2 * i))) | 0x64006400u)
-                                                : ((xs & (0x00030003u << (2 * (i - 5)))) | 0x64006400u);
-                    r[8 * ww + i] = hsub1024(u);
-                }
+                for (int w = 0; w < 8; ++w) r[8 * ii + w] = (i <= 4 ? x[w] : xs[w]) & mask;
             }
         } else {
+            const int ii = chunk;
+            const uint32_t mask = ii <= 1 ? (0x000F000Fu << (4 * ii)) : (0x000F000Fu << (4 * (ii - 2)));
 #pragma unroll
-            for (int ww = 0; ww < 4; ++ww) {
-                const uint32_t x = w[4 * chunk + ww];
-                const uint32_t xs = x >> 8;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t u = (i <= 1) ? ((x & (0x000F000Fu << (4 * i))) | 0x64006400u)
-                                                : ((xs & (0x000F000Fu << (4 * (i - 2)))) | 0x64006400u);
-                    r[4 * ww + i] = hsub1024(u);
-                }
-            }
+            for (int w = 0; w < 16; ++w) r[w] = (ii <= 1 ? x[w] : xs[w]) & mask;
         }
         tc::st16(taddr + 16 * chunk, r);
     }
 }
 
-__device__ __forceinline__ void split_hi_lo(float x, __half& hi, __half& lo) {
-    hi = __float2half_rn(x);
-    lo = __float2half_rn(x - __half2float(hi));
+// Read this thread's packed row (BITS*16 bytes) from shared memory; the 16-byte pieces are read in
+// a thread-dependent rotation so a quarter-warp touches every bank once.
+template <int BITS>
+__device__ __forceinline__ void load_row(const uint8_t* base, int r, uint32_t (&x)[4 * BITS]) {
+    const uint4* p = reinterpret_cast<const uint4*>(base + r * 16 * BITS);
+    if (BITS == 2) {
+        const int sw = (r >> 2) & 1;
+        const uint4 a = p[sw], b = p[sw ^ 1];
+        const uint4 u0 = sw ? b : a, u1 = sw ? a : b;
+        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+    } else {
+        const int rot = (r >> 1) & 3;
+        uint4 u[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) u[q] = p[(q + rot) & 3];
+        // u[q] holds piece (q + rot) & 3: rotate back
+        float4 f0 = *reinterpret_cast<float4*>(&u[0]), f1 = *reinterpret_cast<float4*>(&u[1]);
+        float4 f2 = *reinterpret_cast<float4*>(&u[2]), f3 = *reinterpret_cast<float4*>(&u[3]);
+        rotl4(f0, f1, f2, f3, (4 - rot) & 3);
+        const float4 f[4] = {f0, f1, f2, f3};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x[4 * q] = __float_as_uint(f[q].x);
+            x[4 * q + 1] = __float_as_uint(f[q].y);
+            x[4 * q + 2] = __float_as_uint(f[q].z);
+            x[4 * q + 3] = __float_as_uint(f[q].w);
+        }
+    }
+}
+
+// hi/lo fp16 pieces of GH values, packed as B rows 2h (hi) and 2h+1 (lo); rows >= 2*GH stay zero.
+template <int GH>
+__device__ __forceinline__ void store_b(uint8_t* b, int kk, const float (&x)[GH]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) w[q] = 0u;
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+        const __half hi = __float2half_rn(x[h]);
+        const __half lo = __float2half_rn(x[h] - __half2float(hi));
+        const __half2 v = __halves2half2(hi, lo);
+        w[h] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(b + b_off(0, kk)) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (GH > 4) *reinterpret_cast<uint4*>(b + b_off(8, kk)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Max over the 32 lanes of each of GH values by a transposing butterfly: afterwards every lane of
+// group l >> (5 - log2 GH) holds the maximum of value (l >> (5 - log2 GH)).
+template <int GH>
+__device__ __forceinline__ float warp_max_multi(float (&v)[GH], int lane) {
+    constexpr int kL = GH == 1 ? 0 : (GH == 2 ? 1 : (GH == 4 ? 2 : 3));
+    if (kL >= 1) {
+        constexpr int n = GH / 2;
+        const bool up = lane & 16;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            const float send = up ? v[q] : v[q + n];
+            const float keep = up ? v[q + n] : v[q];
+            v[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+    }
+    if (kL >= 2) {
+        constexpr int n = GH / 4;
+        const bool up = lane & 8;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            const float send = up ? v[q] : v[q + n];
+            const float keep = up ? v[q + n] : v[q];
+            v[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        }
+    }
+    if (kL >= 3) {
+        const bool up = lane & 4;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+    float m = v[0];
+#pragma unroll
+    for (int s = 16 >> kL; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+    return m;
+}
+
+// Sum over the 32 lanes of each of GH values (transposing butterfly, as warp_max_multi): every lane
+// of group l >> (5 - log2 GH) ends with the sum of value (l >> (5 - log2 GH)).
+template <int GH>
+__device__ __forceinline__ float warp_sum_multi(float (&v)[GH], int lane) {
+    constexpr int kL = GH == 1 ? 0 : (GH == 2 ? 1 : (GH == 4 ? 2 : 3));
+    if (kL >= 1) {
+        constexpr int n = GH / 2;
+        const bool up = lane & 16;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            const float send = up ? v[q] : v[q + n];
+            const float keep = up ? v[q + n] : v[q];
+            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+    }
+    if (kL >= 2) {
+        constexpr int n = GH / 4;
+        const bool up = lane & 8;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            const float send = up ? v[q] : v[q + n];
+            const float keep = up ? v[q + n] : v[q];
+            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+    }
+    if (kL >= 3) {
+        const bool up = lane & 4;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    float m = v[0];
+#pragma unroll
+    for (int s = 16 >> kL; s > 0; s >>= 1) m += __shfl_xor_sync(0xffffffffu, m, s);
+    return m;
 }
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -157,269 +276,348 @@ __device__ __forceinline__ bool named_sync_and(int id, int n, bool flag) {
     return out != 0;
 }
 
-template <int KB, int VB>
-struct TileRegs {
-    uint4 k[KB];
-    uint4 v[VB];
-    float s1k, zk, s2k, s1v, zv, s2v, gk, gv;
-};
+// 4-byte asynchronous global -> shared copy, tracked by an mbarrier (which then expects one more
+// arrival from this thread).
+__device__ __forceinline__ void cp_async4_mbar(void* dst, const void* src, uint64_t* bar) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
 
-template <int KB, int VB>
-__device__ __forceinline__ void load_tile(TileRegs<KB, VB>& t, const DecodeArgs& a, int64_t tile, int r) {
-    const uint4* kc = reinterpret_cast<const uint4*>(a.k_codes + tile * (kTile * 16 * KB) + r * (16 * KB));
-    const uint4* vc = reinterpret_cast<const uint4*>(a.v_codes + tile * (kTile * 16 * VB) + r * (16 * VB));
-#pragma unroll
-    for (int u = 0; u < KB; ++u) t.k[u] = __ldg(kc + u);
-#pragma unroll
-    for (int u = 0; u < VB; ++u) t.v[u] = __ldg(vc + u);
-    const uint8_t* kp = a.k_params + tile * KVARN_PARAM_BYTES;
-    const uint8_t* vp = a.v_params + tile * KVARN_PARAM_BYTES;
-    t.s1k = e4m3_value(kp[r]);         // K group scale: channel r
-    t.s2k = e4m3_value(kp[128 + r]);   // K other-axis scale: token r
-    t.zk = fp16_value(reinterpret_cast<const uint16_t*>(kp + 256)[r]);
-    t.s1v = e4m3_value(vp[r]);         // V group scale: token r
-    t.s2v = e4m3_value(vp[128 + r]);   // V other-axis scale: channel r
-    t.zv = fp16_value(reinterpret_cast<const uint16_t*>(vp + 256)[r]);
-    t.gk = a.k_scale[tile];
-    t.gv = a.v_scale[tile];
+// An item = (sequence, kv head, head block, split); items of one worker are consecutive.
+struct Item {
+    int b, kvh, hq0, split, t0, t1;
+};
+__device__ __forceinline__ Item item_at(const DecodeArgs& a, int idx, int hblocks, int gh) {
+    Item it;
+    it.split = idx % a.splits;
+    const int bhk = idx / a.splits;
+    const int hb = bhk % hblocks;
+    const int bk = bhk / hblocks;
+    it.kvh = bk % a.Hkv;
+    it.b = bk / a.Hkv;
+    it.hq0 = it.kvh * a.group + hb * gh;
+    const int n_full = clamp_len(a.seq_lens[it.b], a.max_tiles) >> 7;
+    it.t0 = it.split * kTilesPerSplit;
+    it.t1 = min(it.t0 + kTilesPerSplit, n_full);
+    if (it.t1 < it.t0) it.t1 = it.t0;
+    return it;
 }
 
 template <int KB, int VB, int GH>
 __global__ void __launch_bounds__(kThreads, 2)
-decode_split_kernel(DecodeArgs a) {
+decode_split_kernel(DecodeArgs a, int n_items) {
+    using St = Stage<KB, VB>;
+    constexpr int NS = St::kCount;
     extern __shared__ __align__(1024) uint8_t dsm[];
-    uint8_t* b_all = dsm;                                                  // [WG][2][kBBytes]
-    float* qrs = reinterpret_cast<float*>(dsm + kWG * 2 * kBBytes);        // [GH][128] scaled q'
-    float* einv = qrs + GH * kTile;                                        // [GH] 2^-E_h
-    float* red = einv + 8;                                                 // [WG][3][4 warps][8]
-    float* ms = red + kWG * 3 * 4 * 8;                                     // [WG][GH]
-    float* ls = ms + kWG * GH;                                             // [WG][GH]
-    float* os = ls + kWG * GH;                                             // [WG][GH][128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(os + kWG * GH * kTile);   // [WG]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kWG);
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int wg = warp >> 2, wq = warp & 3, r = tid & 127;
-    const int split = blockIdx.x;
+    const int wk = warp >> 2, wq = warp & 3, r = tid & 127;
+
+    // per-worker shared memory
+    constexpr uint32_t kWorkerBytes = NS * St::kBytes + 2 * kBBytes + GH * kTile * 4 + 8 * 4 + 32 * 4 * 4 +
+                                      2 * kTilesPerSplit * 4 + 16;
+    constexpr uint32_t kWorkerStride = (kWorkerBytes + 1023) & ~1023u;
+    uint8_t* wbase = dsm + wk * kWorkerStride;
+    uint8_t* bk = wbase;                                   // B operands first: 1024-byte aligned
+    uint8_t* bv = bk + kBBytes;
+    uint8_t* stages = bv + kBBytes;
+    float* qrs = reinterpret_cast<float*>(stages + NS * St::kBytes);  // [GH][128]
+    float* einv = qrs + GH * kTile;                        // [8]
+    float* mpart = einv + 8;                               // [4 warps][8]
+    float* lpart = mpart + 32;                             // [4 warps][8]
+    float* zkpart = lpart + 32;                            // [4 warps][8] partial sum_j q' Z_j
+    float* zvpart = zkpart + 32;                           // [4 warps][8] partial sum_t p Zv_t
+    int* tids = reinterpret_cast<int*>(zvpart + 32);       // [2][16]
+    uint8_t* cta = dsm + kWorkers * kWorkerStride;
+    uint64_t* full = reinterpret_cast<uint64_t*>(cta);     // [worker][NS]
+    uint64_t* mmab = full + kWorkers * NS;                 // [worker]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmab + kWorkers);
+
     const int hblocks = a.group / GH;
-    const int kvh = blockIdx.y / hblocks;
-    const int hq0 = kvh * a.group + (blockIdx.y % hblocks) * GH;
-    const int b = blockIdx.z;
-    const int len = clamp_len(a.seq_lens[b], a.max_tiles);
-    const int n_full = len >> 7;
-    const int t_begin = split * kTilesPerSplit;
-    const int t_end = min(t_begin + kTilesPerSplit, n_full);
+    const int n_workers = gridDim.x * kWorkers;
+    const int worker = blockIdx.x * kWorkers + wk;
+    const int i_begin = (int)(((long long)n_items * worker) / n_workers);
+    const int i_end = (int)(((long long)n_items * (worker + 1)) / n_workers);
 
-    if (t_begin >= t_end) {  // nothing to read: empty partials
-        for (int e = tid; e < GH * kTile; e += kThreads) {
-            float* dst = a.ws + (((size_t)b * a.Hq + hq0 + (e >> 7)) * a.splits + split) * kWsStride;
-            dst[4 + (e & 127)] = 0.f;
-            if ((e & 127) == 0) {
-                dst[0] = -INFINITY;
-                dst[1] = 0.f;
-            }
-        }
-        return;
+    for (int i = tid; i < (int)(kWorkers * 2 * kBBytes / 16); i += kThreads) {
+        const int wkr = i / (2 * kBBytes / 16), off = i % (2 * kBBytes / 16);
+        reinterpret_cast<uint4*>(dsm + wkr * kWorkerStride)[off] = make_uint4(0, 0, 0, 0);
     }
-
-    // rotated queries, scaled so that |q'| * 2^E_h <= 2^6 (then q'' = q' S1 <= 2^14 fits fp16)
-    if (warp < GH) {
-        const __nv_bfloat16* qp = a.q + ((size_t)b * a.Hq + hq0 + warp) * kTile + 4 * lane;
-        const uint2 raw = *reinterpret_cast<const uint2*>(qp);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        float v[4] = {f0.x, f0.y, f1.x, f1.y};
-        float sc = a.qscale;
-        if (a.rotate) {
-            fwht128_warp(v, lane);
-            sc *= kInvSqrt128;
-        }
-        float mx = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            v[m] *= sc;
-            mx = fmaxf(mx, fabsf(v[m]));
-        }
-        mx = warp_max(mx);
-        const int e = mx > 0.f ? 6 - ceil_log2(mx) : 0;
-        const float s = ldexpf(1.f, e);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) qrs[warp * kTile + 4 * lane + m] = v[m] * s;
-        if (lane == 0) einv[warp] = ldexpf(1.f, -e);
-    }
-    // B operands: rows 2*GH..15 stay zero
-    for (int i = tid; i < (int)(kWG * 2 * kBBytes / 16); i += kThreads)
-        reinterpret_cast<uint4*>(b_all)[i] = make_uint4(0, 0, 0, 0);
-    if (tid < kWG) mbar_init(&bars[tid], 1);
-    if (warp == 0) tc::alloc(tmem_slot, kWG * kTmemColsPerWG);
+    if (tid < kWorkers * NS) mbar_init(&full[tid], 2);  // the bulk-copy arrival + the cp.async arrival
+    if (tid < kWorkers) mbar_init(&mmab[tid], 1);
+    if (warp == 0) tc::alloc(tmem_slot, kTmemCols);
     fence_mbar_init();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    uint8_t* bk = b_all + wg * 2 * kBBytes;
-    uint8_t* bv = bk + kBBytes;
-    float* cpart = red + wg * 96;   // [4 warps][8]
-    float* mpart = cpart + 32;
-    float* zpart = mpart + 32;
-    const uint32_t col0 = tmem + wg * kTmemColsPerWG;
-    const uint32_t lane_addr = col0 + ((uint32_t)(32 * wq) << 16);  // this thread's TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const uint32_t a_col = tmem + 128 * wk, ds_col = a_col + 64, do_col = a_col + 96;  // D: 2 x 16 each
     const uint32_t bk_addr = smem_addr(bk), bv_addr = smem_addr(bv);
-    constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, 16);
-    const int bar_id = 1 + wg;
-
-    // this thread's slot in the MMA K order: as channel r of a K row, and as token r of a V row
+    const int bar_id = 1 + wk;
+    constexpr uint32_t kIdesc = tc::idesc_f16_f32_bmn(128, 16);
     int kk_k, kk_v;
     float pre_k, pre_v;
-    k_slot<KB>(r, kk_k, pre_k);
-    k_slot<VB>(r, kk_v, pre_v);
+    k_slot<KB>(r, kk_k, pre_k);  // r as channel of a K row
+    k_slot<VB>(r, kk_v, pre_v);  // r as token of a V row
+    const bool producer = (r == 0);
+    const uint64_t bk_desc = tc::smem_desc(bk_addr, kBKStride, kBNStride);
+    const uint64_t bv_desc = tc::smem_desc(bv_addr, kBKStride, kBNStride);
 
-    float m_run[GH], l_part[GH], o[GH];
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-        m_run[h] = -INFINITY;
-        l_part[h] = 0.f;
-        o[h] = 0.f;
+    // ---- producer state (thread r == 0 of the worker): tile ids of the current and next item ----
+    int p_item = i_begin, p_j = 0, p_issued = 0;  // next (item, tile) to issue; tiles issued so far
+    Item p_it;
+    auto issue = [&](int pos) {
+        // bring stream position pos into stage pos % NS
+        const int st = pos % NS;
+        uint8_t* sb = stages + st * St::kBytes;
+        const int64_t tile = tids[(p_item & 1) * kTilesPerSplit + p_j];
+        fence_proxy_async();  // the consumers' reads of this stage come before the TMA writes
+        mbar_expect_tx(&full[wk * NS + st], St::kTx);
+        bulk_g2s(sb + St::kK, a.k_codes + tile * (KB * 2048), KB * 2048, &full[wk * NS + st]);
+        bulk_g2s(sb + St::kV, a.v_codes + tile * (VB * 2048), VB * 2048, &full[wk * NS + st]);
+        bulk_g2s(sb + St::kKP, a.k_params + tile * 512, 512, &full[wk * NS + st]);
+        bulk_g2s(sb + St::kVP, a.v_params + tile * 512, 512, &full[wk * NS + st]);
+        cp_async4(sb + St::kG, a.k_scale + tile);
+        cp_async4_mbar(sb + St::kG + 4, a.v_scale + tile, &full[wk * NS + st]);
+    };
+    auto fetch_tids = [&](int item) {  // tile ids of an item into tids[item & 1] (producer only)
+        if (item >= i_end) return;
+        const Item it = item_at(a, item, hblocks, GH);
+        const int32_t* row = a.block_table + ((size_t)it.b * a.Hkv + it.kvh) * a.max_tiles;
+        for (int j = 0; j < it.t1 - it.t0; ++j) cp_async4(&tids[(item & 1) * kTilesPerSplit + j], row + it.t0 + j);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    // advance the producer to the next item with tiles; returns false at the end of the stream
+    auto producer_advance = [&]() -> bool {
+        while (p_item < i_end) {
+            if (p_j < p_it.t1 - p_it.t0) return true;
+            ++p_item;
+            p_j = 0;
+            if (p_item >= i_end) return false;
+            p_it = item_at(a, p_item, hblocks, GH);
+            asm volatile("cp.async.wait_all;" ::: "memory");  // this item's tile ids have arrived
+            fetch_tids(p_item + 1);
+        }
+        return false;
+    };
+    if (producer && i_begin < i_end) {
+        p_it = item_at(a, i_begin, hblocks, GH);
+        fetch_tids(i_begin);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        fetch_tids(i_begin + 1);
+        for (int s = 0; s < NS; ++s) {
+            if (!producer_advance()) break;
+            issue(p_issued);
+            ++p_issued;
+            ++p_j;
+        }
     }
-    uint32_t phase = 0;
+
+    uint32_t mma_phase = 0;
+    int pos = 0;  // consumer stream position
     bool alive = true;
-    const int32_t* table = a.block_table + ((size_t)b * a.Hkv + kvh) * a.max_tiles;
-
-    TileRegs<KB, VB> cur, nxt;
-    int ti = t_begin + wg;
-    if (ti < t_end) load_tile(cur, a, table[ti], r);
-    for (; ti < t_end && alive; ti += kWG) {
-        if (ti + kWG < t_end) load_tile(nxt, a, table[ti + kWG], r);
-
-        // ---- scores: A = K codes (row r = token r), B = q'' pieces (column r = channel r) ----
-        unpack_row_to_tmem<KB>(cur.k, lane_addr);
-        {
-            const float s1 = cur.s1k * pre_k;
-#pragma unroll
-            for (int h = 0; h < GH; ++h) {
-                __half hi, lo;
-                split_hi_lo(qrs[h * kTile + r] * s1, hi, lo);
-                *reinterpret_cast<__half*>(bk + b_off(2 * h, kk_k)) = hi;
-                *reinterpret_cast<__half*>(bk + b_off(2 * h + 1, kk_k)) = lo;
-                const float c = warp_sum(qrs[h * kTile + r] * cur.zk);
-                if (lane == 0) cpart[wq * 8 + h] = c;
+    for (int item = i_begin; item < i_end && alive; ++item) {
+        const Item it = item_at(a, item, hblocks, GH);
+        const int n_t = it.t1 - it.t0;
+        // rotated queries of this item's heads, scaled so |q'| 2^E <= 2^7 (q' S1 <= 2^15 in fp16)
+        for (int h = wq; h < GH; h += 4) {
+            const __nv_bfloat16* qp = a.q + ((size_t)it.b * a.Hq + it.hq0 + h) * kTile + 4 * lane;
+            const uint2 raw = *reinterpret_cast<const uint2*>(qp);
+            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+            const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+            float v[4] = {f0.x, f0.y, f1.x, f1.y};
+            float sc = a.qscale;
+            if (a.rotate) {
+                fwht128_warp(v, lane);
+                sc *= kInvSqrt128;
             }
-        }
-        fence_proxy_async();
-        tc::wait_st();
-        tc::fence_before();
-        named_sync(bar_id, 128);
-        if (r == 0) {
-            tc::fence_after();
+            float mx = 0.f;
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                tc::mma_f16_ts(col0 + 64, col0 + 8 * s, tc::smem_desc(bk_addr + s * 2 * kLbo, kLbo, kSbo), kIdesc, s > 0);
-            tc::commit(&bars[wg]);
+            for (int m = 0; m < 4; ++m) {
+                v[m] *= sc;
+                mx = fmaxf(mx, fabsf(v[m]));
+            }
+            mx = warp_max(mx);
+            const int e = mx > 0.f ? 7 - ceil_log2(mx) : 0;
+            const float s = ldexpf(1.f, e);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) qrs[h * kTile + 4 * lane + m] = v[m] * s;
+            if (lane == 0) einv[h] = ldexpf(1.f, -e) * kTwo24;  // undo the scale and the 2^-24
         }
-        alive = mbar_wait(&bars[wg], phase, &g_decode_error);
-        phase ^= 1;
-        tc::fence_after();
-        uint32_t d[16];
-        tc::ld16(lane_addr + 64, d);
-        tc::wait_ld();
+        named_sync(bar_id, 128);
 
-        // ---- online softmax over this tile's 128 tokens (thread r = token r), log2 domain ----
-        float s[GH];
+        float m_run[GH], l_part[GH], o[GH];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
-            const float c = cpart[h] + cpart[8 + h] + cpart[16 + h] + cpart[24 + h];
-            s[h] = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1]) + c) * (einv[h] * cur.gk * cur.s2k);
-            const float mx = warp_max(s[h]);
-            if (lane == 0) mpart[wq * 8 + h] = mx;
+            m_run[h] = -INFINITY;
+            l_part[h] = 0.f;
+            o[h] = 0.f;
         }
-        named_sync(bar_id, 128);
-        float alpha[GH];
-#pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            const float mt = fmaxf(fmaxf(mpart[h], mpart[8 + h]), fmaxf(mpart[16 + h], mpart[24 + h]));
-            const float m_new = fmaxf(m_run[h], mt);
-            alpha[h] = exp2f(m_run[h] - m_new);
-            m_run[h] = m_new;
-            const float p = exp2f(s[h] - m_new);
-            l_part[h] = fmaf(l_part[h], alpha[h], p);
-            __half hi, lo;
-            split_hi_lo(p * cur.s1v * (kWScale * pre_v), hi, lo);
-            *reinterpret_cast<__half*>(bv + b_off(2 * h, kk_v)) = hi;
-            *reinterpret_cast<__half*>(bv + b_off(2 * h + 1, kk_v)) = lo;
-            const float z = warp_sum(p * cur.zv);
-            if (lane == 0) zpart[wq * 8 + h] = z;
-        }
+        for (int j = 0; j < n_t && alive; ++j, ++pos) {
+            const int st = pos % NS;
+            const uint8_t* sb = stages + st * St::kBytes;
+            alive = mbar_wait(&full[wk * NS + st], (pos / NS) & 1, &g_decode_error);
+            const float* qv = qrs;
 
-        // ---- PV: A = V codes (row r = channel r), B = p S1 pieces (column r = token r) ----
-        unpack_row_to_tmem<VB>(cur.v, lane_addr);
-        fence_proxy_async();
-        tc::wait_st();
-        tc::fence_before();
-        named_sync(bar_id, 128);
-        if (r == 0) {
-            tc::fence_after();
+            // ---- scores: A = K codes of token r, B = q' S1 2^-shift of channel r ----
+            {
+                uint32_t x[4 * KB];
+                load_row<KB>(sb + St::kK, r, x);
+                unpack_row_to_tmem<KB>(x, a_col + lane_off);
+            }
+            const float gk = *reinterpret_cast<const float*>(sb + St::kG);
+            const float gv = *reinterpret_cast<const float*>(sb + St::kG + 4);
+            {
+                float xs[GH], xz[GH];
+                const float s1 = e4m3_value(sb[St::kKP + r]) * pre_k;
+                const float z = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kKP + 256)[r]);
 #pragma unroll
-            for (int s2 = 0; s2 < 8; ++s2)
-                tc::mma_f16_ts(col0 + 96, col0 + 8 * s2, tc::smem_desc(bv_addr + s2 * 2 * kLbo, kLbo, kSbo), kIdesc, s2 > 0);
-            tc::commit(&bars[wg]);
-        }
-        alive = mbar_wait(&bars[wg], phase, &g_decode_error) && alive;
-        phase ^= 1;
-        tc::fence_after();
-        tc::ld16(lane_addr + 96, d);
-        tc::wait_ld();
-        {
-            const float sc = cur.gv * cur.s2v;  // channel r
+                for (int h = 0; h < GH; ++h) {
+                    const float q = qv[h * kTile + r];
+                    xs[h] = q * s1;
+                    xz[h] = q * z;
+                }
+                store_b<GH>(bk, kk_k, xs);
+                // sum_j q'_j Z_j: per-warp partials, combined after the barrier below
+                const float zsum = warp_sum_multi<GH>(xz, lane);
+                constexpr int kGroup = 32 / GH;
+                if ((lane & (kGroup - 1)) == 0) zkpart[wq * 8 + lane / kGroup] = zsum;
+            }
+            fence_proxy_async();
+            tc::wait_st();
+            tc::fence_before();
+            named_sync(bar_id, 128);
+            if (producer) {
+                tc::fence_after();
+                // two independent accumulation chains (even / odd K steps) halve the chain latency
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    tc::mma_f16_ts(ds_col + 16 * (s & 1), a_col + 8 * s, bk_desc + (uint64_t)(s * 2 * kBKStride >> 4),
+                                   kIdesc, s > 1);
+                tc::commit(&mmab[wk]);
+            }
+            alive = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && alive;
+            mma_phase ^= 1;
+            tc::fence_after();
+            uint32_t d[16], d2[16];
+            tc::ld16(ds_col + lane_off, d);
+            tc::ld16(ds_col + 16 + lane_off, d2);
+            tc::wait_ld();
+
+            // ---- online softmax over the tile's 128 tokens (thread r = token r), log2 domain ----
+            float sc[GH], mx[GH];
+            const float tok = gk * e4m3_value(sb[St::kKP + 128 + r]);
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
-                const float z = zpart[h] + zpart[8 + h] + zpart[16 + h] + zpart[24 + h];
-                const float acc = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) * (1.f / kWScale) + z;
-                o[h] = fmaf(o[h], alpha[h], acc * sc);
+                const float zk = (zkpart[h] + zkpart[8 + h]) + (zkpart[16 + h] + zkpart[24 + h]);
+                const float dot = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) +
+                                  (__uint_as_float(d2[2 * h]) + __uint_as_float(d2[2 * h + 1]));
+                sc[h] = fmaf(dot, einv[h], zk * (einv[h] * (1.f / kTwo24))) * tok;
+                mx[h] = sc[h];
+            }
+            {
+                const float m = warp_max_multi<GH>(mx, lane);
+                constexpr int kGroup = 32 / GH;
+                if ((lane & (kGroup - 1)) == 0) mpart[wq * 8 + lane / kGroup] = m;
+            }
+            named_sync(bar_id, 128);
+            float alpha[GH];
+            {
+                float xs[GH], xz[GH];
+                const float w = e4m3_value(sb[St::kVP + r]) * (kWScale * pre_v);
+                const float z = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kVP + 256)[r]);
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    const float mt = fmaxf(fmaxf(mpart[h], mpart[8 + h]), fmaxf(mpart[16 + h], mpart[24 + h]));
+                    const float m_new = fmaxf(m_run[h], mt);
+                    alpha[h] = exp2f(m_run[h] - m_new);
+                    m_run[h] = m_new;
+                    const float p = exp2f(sc[h] - m_new);
+                    l_part[h] = fmaf(l_part[h], alpha[h], p);
+                    xs[h] = p * w;
+                    xz[h] = p * z;
+                }
+                store_b<GH>(bv, kk_v, xs);
+                // sum_t p_t Zv_t: per-warp partials, combined after the barrier below
+                const float zsum = warp_sum_multi<GH>(xz, lane);
+                constexpr int kGroup = 32 / GH;
+                if ((lane & (kGroup - 1)) == 0) zvpart[wq * 8 + lane / kGroup] = zsum;
+            }
+
+            // ---- PV: A = V codes of channel r, B = p S1 2^-shift of token r ----
+            {
+                uint32_t x[4 * VB];
+                load_row<VB>(sb + St::kV, r, x);
+                unpack_row_to_tmem<VB>(x, a_col + lane_off);
+            }
+            const float chan = gv * e4m3_value(sb[St::kVP + 128 + r]);  // channel r
+            fence_proxy_async();
+            tc::wait_st();
+            tc::fence_before();
+            named_sync(bar_id, 128);
+            if (producer) {
+                tc::fence_after();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    tc::mma_f16_ts(do_col + 16 * (s & 1), a_col + 8 * s, bv_desc + (uint64_t)(s * 2 * kBKStride >> 4),
+                                   kIdesc, s > 1);
+                tc::commit(&mmab[wk]);
+            }
+            alive = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && alive;
+            mma_phase ^= 1;
+            tc::fence_after();
+            tc::ld16(do_col + lane_off, d);
+            tc::ld16(do_col + 16 + lane_off, d2);
+            tc::wait_ld();
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                const float zv = (zvpart[h] + zvpart[8 + h]) + (zvpart[16 + h] + zvpart[24 + h]);
+                const float acc = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) +
+                                  (__uint_as_float(d2[2 * h]) + __uint_as_float(d2[2 * h + 1]));
+                o[h] = fmaf(o[h], alpha[h], fmaf(acc, kTwo24 / kWScale, zv) * chan);
+            }
+            // the stage, B, mpart and TMEM of this tile are free once every thread is here; the
+            // barrier also makes the give-up decision uniform
+            tc::fence_before();
+            alive = named_sync_and(bar_id, 128, alive);
+            tc::fence_after();
+            if (producer && alive && producer_advance()) {
+                issue(p_issued);
+                ++p_issued;
+                ++p_j;
             }
         }
-        cur = nxt;
-        // the scratch (cpart/mpart/zpart, B) of this tile is reused by the next: all threads must
-        // be past their reads; the barrier also makes the give-up decision uniform
-        tc::fence_before();
-        alive = named_sync_and(bar_id, 128, alive);
-        tc::fence_after();
+
+        // ---- this item's partial (m, l, o) for its heads ----
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            const float ls = warp_sum(l_part[h]);
+            if (lane == 0) lpart[wq * 8 + h] = ls;
+        }
+        named_sync(bar_id, 128);
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            float* dst = a.ws + (((size_t)it.b * a.Hq + it.hq0 + h) * a.splits + it.split) * kWsStride;
+            dst[4 + r] = o[h];
+            if (r == 0) {
+                dst[0] = m_run[h];
+                dst[1] = lpart[h] + lpart[8 + h] + lpart[16 + h] + lpart[24 + h];
+            }
+        }
+        named_sync(bar_id, 128);  // lpart / qrs are rewritten by the next item
     }
-
-    // ---- merge the warpgroups of this CTA ----
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-        const float lsum = warp_sum(l_part[h]);
-        if (lane == 0) red[wg * 96 + wq * 8 + h] = lsum;
-        os[(wg * GH + h) * kTile + r] = o[h];
-        if (r == 0) ms[wg * GH + h] = m_run[h];
+    if (producer) {
+        // after a give-up, wait (bounded) for copies still in flight before the CTA exits
+        for (int q = pos; q < p_issued; ++q) mbar_wait(&full[wk * NS + q % NS], (q / NS) & 1, &g_decode_error);
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     tc::fence_before();
     __syncthreads();
-    for (int e = tid; e < GH * kTile; e += kThreads) {
-        const int h = e >> 7, j = e & 127;
-        float mmax = -INFINITY;
-#pragma unroll
-        for (int g = 0; g < kWG; ++g) mmax = fmaxf(mmax, ms[g * GH + h]);
-        float ov = 0.f, l = 0.f;
-        if (mmax != -INFINITY) {
-#pragma unroll
-            for (int g = 0; g < kWG; ++g) {
-                const float f = exp2f(ms[g * GH + h] - mmax);
-                const float lg = red[g * 96 + h] + red[g * 96 + 8 + h] + red[g * 96 + 16 + h] + red[g * 96 + 24 + h];
-                ov = fmaf(os[(g * GH + h) * kTile + j], f, ov);
-                l = fmaf(lg, f, l);
-            }
-        }
-        float* dst = a.ws + (((size_t)b * a.Hq + hq0 + h) * a.splits + split) * kWsStride;
-        dst[4 + j] = ov;
-        if (j == 0) {
-            dst[0] = mmax;
-            dst[1] = l;
-        }
-    }
     tc::fence_after();
-    if (warp == 0) tc::dealloc(tmem, kWG * kTmemColsPerWG);
+    if (warp == 0) tc::dealloc(tmem, kTmemCols);
 }
 
 // One warp per (sequence, query head): merge splits, inverse rotation, bf16 tail, normalise.
@@ -479,30 +677,40 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + hq) * kTile + 4 * lane) = r;
 }
 
-template <int GH>
+template <int KB, int VB, int GH>
 size_t split_smem_bytes() {
-    size_t bytes = (size_t)kWG * 2 * kBBytes + (size_t)GH * kTile * 4 + 8 * 4 + kWG * 3 * 4 * 8 * 4 +
-                   2 * kWG * GH * 4 + (size_t)kWG * GH * kTile * 4 + kWG * 8 + 16;
+    using St = Stage<KB, VB>;
+    constexpr uint32_t kWorkerBytes = St::kCount * St::kBytes + 2 * kBBytes + GH * kTile * 4 + 8 * 4 + 32 * 4 * 4 +
+                                      2 * kTilesPerSplit * 4 + 16;
+    constexpr uint32_t kWorkerStride = (kWorkerBytes + 1023) & ~1023u;
+    size_t bytes = (size_t)kWorkers * kWorkerStride + kWorkers * St::kCount * 8 + kWorkers * 8 + 16;
     // at least 80 KB, so no more than two CTAs (2 x 256 TMEM columns) share an SM
     return bytes < 80 * 1024 ? 80 * 1024 : bytes;
 }
 
 template <int KB, int VB, int GH>
-cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
+cudaError_t run_split(const DecodeArgs& a, int n_items, cudaStream_t stream) {
     auto kern = decode_split_kernel<KB, VB, GH>;
-    const size_t smem = split_smem_bytes<GH>();
+    const size_t smem = split_smem_bytes<KB, VB, GH>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(a);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int want = (n_items + kWorkers - 1) / kWorkers;
+    const int grid = want < 2 * sms ? want : 2 * sms;  // persistent: two CTAs per SM
+    kern<<<grid, kThreads, smem, stream>>>(a, n_items);
     return cudaGetLastError();
 }
 
 template <int KB, int VB>
-cudaError_t run_split_g(const DecodeArgs& a, int gh, dim3 grid, cudaStream_t stream) {
-    if (gh == 1) return run_split<KB, VB, 1>(a, grid, stream);
-    if (gh == 2) return run_split<KB, VB, 2>(a, grid, stream);
-    if (gh == 4) return run_split<KB, VB, 4>(a, grid, stream);
-    return run_split<KB, VB, 8>(a, grid, stream);
+cudaError_t run_split_g(const DecodeArgs& a, int gh, int n_items, cudaStream_t stream) {
+    if (gh == 1) return run_split<KB, VB, 1>(a, n_items, stream);
+    if (gh == 2) return run_split<KB, VB, 2>(a, n_items, stream);
+    if (gh == 4) return run_split<KB, VB, 4>(a, n_items, stream);
+    return run_split<KB, VB, 8>(a, n_items, stream);
 }
 
 }  // namespace
@@ -553,12 +761,12 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.ws = static_cast<float*>(workspace);
     a.out = out;
     const int gh = group;  // up to 8 heads x (hi, lo) fill the 16 MMA columns
-    dim3 grid(plan.splits, Hkv * (group / gh), B);
+    const int n_items = B * Hkv * (group / gh) * plan.splits;
     cudaError_t e;
-    if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, grid, stream);
-    else if (k_bits == 4 && v_bits == 2) e = run_split_g<4, 2>(a, gh, grid, stream);
-    else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, grid, stream);
-    else e = run_split_g<4, 4>(a, gh, grid, stream);
+    if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, n_items, stream);
+    else if (k_bits == 4 && v_bits == 2) e = run_split_g<4, 2>(a, gh, n_items, stream);
+    else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, n_items, stream);
+    else e = run_split_g<4, 4>(a, gh, n_items, stream);
     if (e != cudaSuccess) return e;
     decode_merge_kernel<<<dim3(Hq, B), 32, 0, stream>>>(a);
     return cudaGetLastError();

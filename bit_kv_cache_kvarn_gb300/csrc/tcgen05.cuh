@@ -42,8 +42,8 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
-// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of 8 rows x 16 bytes;
-// lbo = byte stride between core matrices along K, sbo = along M/N.
+// Shared-memory matrix descriptor, no swizzle: core matrices of 8 rows x 16 bytes; lbo = byte
+// stride between core matrices along K, sbo = along M/N (for both K-major and MN-major B).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
            (1ull << 46);
@@ -52,6 +52,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 // Instruction descriptor for kind::f16 with fp16 A and B (K-major) and an fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// Same with B stored MN-major (N contiguous): core matrices of 8 K-rows x 16 bytes.
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int m, int n) {
+    return idesc_f16_f32(m, n) | (1u << 16);
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.
