@@ -46,7 +46,10 @@ constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, 
 constexpr uint32_t kTmemCols = 256;         // worker w: A (64), D_S (2 x 16), D_O (2 x 16) at 128 w
 constexpr uint32_t kBBytes = 256 * 16 * 2;  // one B operand: K = 256 x N = 16 fp16, N-contiguous
 constexpr uint32_t kBKStride = 256, kBNStride = 128;  // core-matrix strides of B along K and N
-constexpr float kWScale = 32.f;             // p S1 <= 256 -> x32 stays inside fp16
+// Lazy maximum: keep the running max while no score exceeds it by more than kLazy (log2 units), so
+// p <= 2^kLazy; with S1 <= 256, p S1 kWScale <= 2^15 fits fp16 while small terms stay normal.
+constexpr float kLazy = 4.f;
+constexpr float kWScale = 8.f;
 constexpr float kTwo24 = 16777216.f;
 
 struct DecodeArgs {
@@ -265,6 +268,16 @@ __device__ __forceinline__ float warp_sum_multi(float (&v)[GH], int lane) {
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// Barrier over n threads that also returns the OR of every thread's flag.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool flag) {
+    uint32_t out;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n bar.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(out)
+        : "r"(id), "r"(n), "r"((uint32_t)flag)
+        : "memory");
+    return out != 0;
+}
 // Barrier over n threads that also returns the AND of every thread's flag.
 __device__ __forceinline__ bool named_sync_and(int id, int n, bool flag) {
     uint32_t out;
@@ -417,8 +430,9 @@ decode_split_kernel(DecodeArgs a, int n_items) {
     }
 
     uint32_t mma_phase = 0;
-    int pos = 0;  // consumer stream position
-    bool alive = true;
+    int pos = 0;       // consumer stream position
+    bool ok = true;    // this thread's waits all succeeded
+    bool alive = true;  // uniform over the worker: changes only at AND-barriers
     for (int item = i_begin; item < i_end && alive; ++item) {
         const Item it = item_at(a, item, hblocks, GH);
         const int n_t = it.t1 - it.t0;
@@ -459,7 +473,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
         for (int j = 0; j < n_t && alive; ++j, ++pos) {
             const int st = pos % NS;
             const uint8_t* sb = stages + st * St::kBytes;
-            alive = mbar_wait(&full[wk * NS + st], (pos / NS) & 1, &g_decode_error);
+            ok = mbar_wait(&full[wk * NS + st], (pos / NS) & 1, &g_decode_error) && ok;
             const float* qv = qrs;
 
             // ---- scores: A = K codes of token r, B = q' S1 2^-shift of channel r ----
@@ -489,7 +503,10 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             fence_proxy_async();
             tc::wait_st();
             tc::fence_before();
-            named_sync(bar_id, 128);
+            // this barrier also orders every reuse of the previous tile's stage, B, scratch and TMEM,
+            // and makes the give-up decision uniform
+            alive = named_sync_and(bar_id, 128, ok && alive);
+            if (!alive) break;
             if (producer) {
                 tc::fence_after();
                 // two independent accumulation chains (even / odd K steps) halve the chain latency
@@ -498,8 +515,15 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                     tc::mma_f16_ts(ds_col + 16 * (s & 1), a_col + 8 * s, bk_desc + (uint64_t)(s * 2 * kBKStride >> 4),
                                    kIdesc, s > 1);
                 tc::commit(&mmab[wk]);
+                // while the MMAs run: refill the stage the previous tile used (every thread of the
+                // worker is past it: they all reached the barrier above)
+                if (pos > 0 && alive && producer_advance()) {
+                    issue(p_issued);
+                    ++p_issued;
+                    ++p_j;
+                }
             }
-            alive = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && alive;
+            ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
             tc::fence_after();
             uint32_t d[16], d2[16];
@@ -508,44 +532,40 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             tc::wait_ld();
 
             // ---- online softmax over the tile's 128 tokens (thread r = token r), log2 domain ----
-            float sc[GH], mx[GH];
+            // Lazy maximum: p = 2^(s - m) with the running maximum m while no score of the tile
+            // exceeds it by more than kLazy (p <= 2^kLazy keeps p S1 kWScale inside fp16); otherwise
+            // (always on an item's first tile) the tile maximum is taken exactly and the partial
+            // sums are rescaled.
+            float sc[GH], p[GH];
             const float tok = gk * e4m3_value(sb[St::kKP + 128 + r]);
+            bool over = false;
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 const float zk = (zkpart[h] + zkpart[8 + h]) + (zkpart[16 + h] + zkpart[24 + h]);
                 const float dot = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) +
                                   (__uint_as_float(d2[2 * h]) + __uint_as_float(d2[2 * h + 1]));
                 sc[h] = fmaf(dot, einv[h], zk * (einv[h] * (1.f / kTwo24))) * tok;
-                mx[h] = sc[h];
+                over = over || !(sc[h] <= m_run[h] + kLazy);
+                p[h] = exp2f(sc[h] - m_run[h]);
             }
-            {
-                const float m = warp_max_multi<GH>(mx, lane);
-                constexpr int kGroup = 32 / GH;
-                if ((lane & (kGroup - 1)) == 0) mpart[wq * 8 + lane / kGroup] = m;
-            }
-            named_sync(bar_id, 128);
-            float alpha[GH];
-            {
+            const float w = e4m3_value(sb[St::kVP + r]) * (kWScale * pre_v);
+            const float zval = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kVP + 256)[r]);
+            auto build_bv = [&]() {
                 float xs[GH], xz[GH];
-                const float w = e4m3_value(sb[St::kVP + r]) * (kWScale * pre_v);
-                const float z = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kVP + 256)[r]);
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    const float mt = fmaxf(fmaxf(mpart[h], mpart[8 + h]), fmaxf(mpart[16 + h], mpart[24 + h]));
-                    const float m_new = fmaxf(m_run[h], mt);
-                    alpha[h] = exp2f(m_run[h] - m_new);
-                    m_run[h] = m_new;
-                    const float p = exp2f(sc[h] - m_new);
-                    l_part[h] = fmaf(l_part[h], alpha[h], p);
-                    xs[h] = p * w;
-                    xz[h] = p * z;
+                    xs[h] = p[h] * w;
+                    xz[h] = p[h] * zval;
                 }
                 store_b<GH>(bv, kk_v, xs);
                 // sum_t p_t Zv_t: per-warp partials, combined after the barrier below
                 const float zsum = warp_sum_multi<GH>(xz, lane);
                 constexpr int kGroup = 32 / GH;
                 if ((lane & (kGroup - 1)) == 0) zvpart[wq * 8 + lane / kGroup] = zsum;
-            }
+            };
+            // build_bv shuffles across the warp, so the choice must be warp-uniform; any warp with an
+            // overflowing lane leaves it to the exact path (the OR below then is true as well)
+            if (!__any_sync(0xffffffffu, over)) build_bv();
 
             // ---- PV: A = V codes of channel r, B = p S1 2^-shift of token r ----
             {
@@ -554,6 +574,32 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                 unpack_row_to_tmem<VB>(x, a_col + lane_off);
             }
             const float chan = gv * e4m3_value(sb[St::kVP + 128 + r]);  // channel r
+            if (named_sync_or(bar_id, 128, over)) {
+                // exact tile maximum, rescale, rebuild B
+                float mx[GH];
+#pragma unroll
+                for (int h = 0; h < GH; ++h) mx[h] = sc[h];
+                {
+                    const float m = warp_max_multi<GH>(mx, lane);
+                    constexpr int kGroup = 32 / GH;
+                    if ((lane & (kGroup - 1)) == 0) mpart[wq * 8 + lane / kGroup] = m;
+                }
+                named_sync(bar_id, 128);
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    const float mt = fmaxf(fmaxf(mpart[h], mpart[8 + h]), fmaxf(mpart[16 + h], mpart[24 + h]));
+                    const float m_new = fmaxf(m_run[h], mt);
+                    const float alpha = exp2f(m_run[h] - m_new);
+                    m_run[h] = m_new;
+                    l_part[h] *= alpha;
+                    o[h] *= alpha;
+                    p[h] = exp2f(sc[h] - m_new);
+                }
+                build_bv();
+                named_sync(bar_id, 128);  // mpart is read; zvpart and B are complete
+            }
+#pragma unroll
+            for (int h = 0; h < GH; ++h) l_part[h] += p[h];
             fence_proxy_async();
             tc::wait_st();
             tc::fence_before();
@@ -566,7 +612,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                                    kIdesc, s > 1);
                 tc::commit(&mmab[wk]);
             }
-            alive = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && alive;
+            ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
             tc::fence_after();
             tc::ld16(do_col + lane_off, d);
@@ -577,17 +623,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                 const float zv = (zvpart[h] + zvpart[8 + h]) + (zvpart[16 + h] + zvpart[24 + h]);
                 const float acc = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) +
                                   (__uint_as_float(d2[2 * h]) + __uint_as_float(d2[2 * h + 1]));
-                o[h] = fmaf(o[h], alpha[h], fmaf(acc, kTwo24 / kWScale, zv) * chan);
-            }
-            // the stage, B, mpart and TMEM of this tile are free once every thread is here; the
-            // barrier also makes the give-up decision uniform
-            tc::fence_before();
-            alive = named_sync_and(bar_id, 128, alive);
-            tc::fence_after();
-            if (producer && alive && producer_advance()) {
-                issue(p_issued);
-                ++p_issued;
-                ++p_j;
+                o[h] = fmaf(fmaf(acc, kTwo24 / kWScale, zv), chan, o[h]);
             }
         }
 
@@ -597,7 +633,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             const float ls = warp_sum(l_part[h]);
             if (lane == 0) lpart[wq * 8 + h] = ls;
         }
-        named_sync(bar_id, 128);
+        alive = named_sync_and(bar_id, 128, ok && alive);
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             float* dst = a.ws + (((size_t)it.b * a.Hq + it.hq0 + h) * a.splits + it.split) * kWsStride;
@@ -611,7 +647,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
     }
     if (producer) {
         // after a give-up, wait (bounded) for copies still in flight before the CTA exits
-        for (int q = pos; q < p_issued; ++q) mbar_wait(&full[wk * NS + q % NS], (q / NS) & 1, &g_decode_error);
+        for (int q = pos; q < p_issued; ++q) mbar_drain(&full[wk * NS + q % NS], (q / NS) & 1);
         asm volatile("cp.async.wait_all;" ::: "memory");
     }
     tc::fence_before();

@@ -114,6 +114,14 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
         const int buf = local & 1;
         const bool ok_data = mbar_wait(&sm.bar[buf], (local >> 1) & 1, &g_encode_error);
+        if (!__syncthreads_and(ok_data)) {
+            // a copy never arrived (the error word is set): wait for this CTA's copies, then stop
+            if (tid == 0) {
+                mbar_drain(&sm.bar[buf], (local >> 1) & 1);
+                if (tile + gridDim.x < n_tiles) mbar_drain(&sm.bar[buf ^ 1], ((local + 1) >> 1) & 1);
+            }
+            break;
+        }
         const __nv_bfloat16* xs = sm.xs[buf];
 
         // ---- rotation pass 1: H_16 over channel bits 0..3, 16 contiguous channels per item ----

@@ -83,10 +83,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
-// Wait for the phase with the given parity; bounded: on timeout sets *err_word and returns false
-// (the caller then skips the work that needed the data).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the mbarrier phase with the given parity.  Bounded: gives up after kWaitNs of wall time
+// (or kSpinLimit polls), sets *err_word and returns false; once *err_word is set by any thread of
+// the grid, every later wait returns false at once, so a stuck kernel ends within about a second.
+constexpr uint64_t kWaitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err_word) {
-    uint32_t addr = smem_addr(bar);
+    const uint32_t addr = smem_addr(bar);
+    uint64_t t0 = 0;
     for (long long i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
         asm volatile(
@@ -95,9 +104,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
             : "r"(addr), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((i & 255) == 0) {
+            if (*reinterpret_cast<volatile unsigned int*>(err_word)) return false;
+            const uint64_t t = global_ns();
+            if (i == 0) t0 = t;
+            else if (t - t0 > kWaitNs) break;
+        }
     }
     atomicOr(err_word, kErrTmaTimeout);
     return false;
+}
+
+// After a give-up: wait (bounded by time only) for a copy this CTA issued, so it never exits with a
+// bulk copy still writing into its shared memory.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_addr(bar);
+    const uint64_t t0 = global_ns();
+    for (long long i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done || ((i & 255) == 0 && global_ns() - t0 > kWaitNs)) return;
+    }
 }
 
 // ---- Hadamard butterflies in registers ---------------------------------------------------------
