@@ -17,13 +17,14 @@
 //     and stores them in TMEM as the MMA's A operand;
 //   * writes q'' = q' S1 2^-shift for channel r as fp16 hi/lo pieces into the B operand (shared
 //     memory, N-contiguous) -- up to 8 heads x 2 pieces = N 16 -- and its share of sum_j q'_j Z_j;
-//   * after 8 tcgen05.mma (two independent accumulation chains), owns token r's scores, runs the
-//     online softmax (log2 domain), writes p S1 for token r as the next B and its share of
-//     sum_t p_t Z_t, masks V row r (channel r) into A, and after 8 more MMAs owns channel r of
-//     sum_t p_t v_t.
-// The number and depth of MMA instructions, not their FLOPs, set the tensor-core cost here (a
-// dependent K=16 step costs ~200 cycles; N up to 64 costs nothing extra), hence the zero-point
-// sums on the CUDA cores and the two chains.
+//   * after 8 tcgen05.mma, owns token r's scores, runs the online softmax (log2 domain), writes
+//     p S1 for token r as the next B and its share of sum_t p_t Z_t, masks V row r (channel r)
+//     into A, and after 8 more MMAs owns channel r of sum_t p_t v_t.
+// The number of MMA instructions per issuing warp, not their FLOPs, sets the tensor-core cost
+// here: one warp's MMAs complete one after another (~130 cycles each for M=128, K=16, whatever N
+// and whether or not they share an accumulator), while MMAs issued by different warps overlap.
+// So each of the worker's 4 warps issues 2 of the 8 K-steps into its own 16-column partial
+// accumulator and the partials are summed on readout; the zero-point sums stay on the CUDA cores.
 // Merge kernel: one warp per (sequence, query head) merges the items by log-sum-exp, applies the
 // inverse rotation, attends to the unquantised bf16 tail and normalises.
 #include <math.h>
@@ -43,7 +44,7 @@ constexpr int kThreads = 256;
 constexpr int kWorkers = 2;                 // warpgroups per CTA
 constexpr int kTilesPerSplit = 16;
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
-constexpr uint32_t kTmemCols = 256;         // worker w: A (64), D_S (2 x 16), D_O (2 x 16) at 128 w
+constexpr uint32_t kTmemCols = 256;         // worker w: A (64) and D (4 partials x 16) at 128 w
 constexpr uint32_t kBBytes = 256 * 16 * 2;  // one B operand: K = 256 x N = 16 fp16, N-contiguous
 constexpr uint32_t kBKStride = 256, kBNStride = 128;  // core-matrix strides of B along K and N
 // Lazy maximum: keep the running max while no score exceeds it by more than kLazy (log2 units), so
@@ -265,6 +266,42 @@ __device__ __forceinline__ float warp_sum_multi(float (&v)[GH], int lane) {
     return m;
 }
 
+// tcgen05.ld of NC consecutive 32-bit columns (32x32b shape; NC = 2, 4, 8 or 16).
+template <int NC>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, uint32_t (&r)[NC]) {
+    if constexpr (NC == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
+    } else if constexpr (NC == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
+    } else if constexpr (NC == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr) : "memory");
+    } else {
+        tc::ld16(taddr, r);
+    }
+}
+
+// Sum of the 4 partial accumulators (16 columns apart) for the 2*GH used columns: acc[2h] is head
+// h's hi piece, acc[2h+1] its lo piece.
+template <int GH>
+__device__ __forceinline__ void read_partials(uint32_t d_taddr, float (&acc)[2 * GH]) {
+    constexpr int NC = 2 * GH;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t r0[NC], r1[NC];
+        ld_cols<NC>(d_taddr + 32 * half, r0);
+        ld_cols<NC>(d_taddr + 32 * half + 16, r1);
+        tc::wait_ld();
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const float v = __uint_as_float(r0[c]) + __uint_as_float(r1[c]);
+            acc[c] = half ? acc[c] + v : v;
+        }
+    }
+}
+
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -359,7 +396,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
         reinterpret_cast<uint4*>(dsm + wkr * kWorkerStride)[off] = make_uint4(0, 0, 0, 0);
     }
     if (tid < kWorkers * NS) mbar_init(&full[tid], 2);  // the bulk-copy arrival + the cp.async arrival
-    if (tid < kWorkers) mbar_init(&mmab[tid], 1);
+    if (tid < kWorkers) mbar_init(&mmab[tid], 4);  // one tcgen05.commit per warp of the worker
     if (warp == 0) tc::alloc(tmem_slot, kTmemCols);
     fence_mbar_init();
     tc::fence_before();
@@ -367,7 +404,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
-    const uint32_t a_col = tmem + 128 * wk, ds_col = a_col + 64, do_col = a_col + 96;  // D: 2 x 16 each
+    const uint32_t a_col = tmem + 128 * wk, d_col = a_col + 64;  // D: 4 partials x 16 columns
     const uint32_t bk_addr = smem_addr(bk), bv_addr = smem_addr(bv);
     const int bar_id = 1 + wk;
     constexpr uint32_t kIdesc = tc::idesc_f16_f32_bmn(128, 16);
@@ -507,14 +544,18 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             // and makes the give-up decision uniform
             alive = named_sync_and(bar_id, 128, ok && alive);
             if (!alive) break;
-            if (producer) {
+            if (lane == 0) {
+                // warp wq issues K-steps 2 wq and 2 wq + 1 into its own partial accumulator
                 tc::fence_after();
-                // two independent accumulation chains (even / odd K steps) halve the chain latency
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    tc::mma_f16_ts(ds_col + 16 * (s & 1), a_col + 8 * s, bk_desc + (uint64_t)(s * 2 * kBKStride >> 4),
-                                   kIdesc, s > 1);
+                for (int u = 0; u < 2; ++u) {
+                    const int s = 2 * wq + u;
+                    tc::mma_f16_ts(d_col + 16 * wq, a_col + 8 * s, bk_desc + (uint64_t)(s * 2 * kBKStride >> 4),
+                                   kIdesc, u);
+                }
                 tc::commit(&mmab[wk]);
+            }
+            if (producer) {
                 // while the MMAs run: refill the stage the previous tile used (every thread of the
                 // worker is past it: they all reached the barrier above)
                 if (pos > 0 && alive && producer_advance()) {
@@ -526,10 +567,8 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
             tc::fence_after();
-            uint32_t d[16], d2[16];
-            tc::ld16(ds_col + lane_off, d);
-            tc::ld16(ds_col + 16 + lane_off, d2);
-            tc::wait_ld();
+            float dsum[2 * GH];
+            read_partials<GH>(d_col + lane_off, dsum);
 
             // ---- online softmax over the tile's 128 tokens (thread r = token r), log2 domain ----
             // Lazy maximum: p = 2^(s - m) with the running maximum m while no score of the tile
@@ -542,8 +581,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 const float zk = (zkpart[h] + zkpart[8 + h]) + (zkpart[16 + h] + zkpart[24 + h]);
-                const float dot = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) +
-                                  (__uint_as_float(d2[2 * h]) + __uint_as_float(d2[2 * h + 1]));
+                const float dot = dsum[2 * h] + dsum[2 * h + 1];
                 sc[h] = fmaf(dot, einv[h], zk * (einv[h] * (1.f / kTwo24))) * tok;
                 over = over || !(sc[h] <= m_run[h] + kLazy);
                 p[h] = exp2f(sc[h] - m_run[h]);
@@ -574,6 +612,11 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                 unpack_row_to_tmem<VB>(x, a_col + lane_off);
             }
             const float chan = gv * e4m3_value(sb[St::kVP + 128 + r]);  // channel r
+            fence_proxy_async();
+            tc::wait_st();
+            tc::fence_before();
+            // one barrier when no score overshot the lazy maximum: A, B and the partial sums are
+            // then complete; otherwise the exact path below adds two
             if (named_sync_or(bar_id, 128, over)) {
                 // exact tile maximum, rescale, rebuild B
                 float mx[GH];
@@ -596,33 +639,30 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                     p[h] = exp2f(sc[h] - m_new);
                 }
                 build_bv();
+                fence_proxy_async();
+                tc::fence_before();
                 named_sync(bar_id, 128);  // mpart is read; zvpart and B are complete
             }
 #pragma unroll
             for (int h = 0; h < GH; ++h) l_part[h] += p[h];
-            fence_proxy_async();
-            tc::wait_st();
-            tc::fence_before();
-            named_sync(bar_id, 128);
-            if (producer) {
+            if (lane == 0) {
                 tc::fence_after();
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    tc::mma_f16_ts(do_col + 16 * (s & 1), a_col + 8 * s, bv_desc + (uint64_t)(s * 2 * kBKStride >> 4),
-                                   kIdesc, s > 1);
+                for (int u = 0; u < 2; ++u) {
+                    const int s = 2 * wq + u;
+                    tc::mma_f16_ts(d_col + 16 * wq, a_col + 8 * s, bv_desc + (uint64_t)(s * 2 * kBKStride >> 4),
+                                   kIdesc, u);
+                }
                 tc::commit(&mmab[wk]);
             }
             ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
             tc::fence_after();
-            tc::ld16(do_col + lane_off, d);
-            tc::ld16(do_col + 16 + lane_off, d2);
-            tc::wait_ld();
+            read_partials<GH>(d_col + lane_off, dsum);
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 const float zv = (zvpart[h] + zvpart[8 + h]) + (zvpart[16 + h] + zvpart[24 + h]);
-                const float acc = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) +
-                                  (__uint_as_float(d2[2 * h]) + __uint_as_float(d2[2 * h + 1]));
+                const float acc = dsum[2 * h] + dsum[2 * h + 1];
                 o[h] = fmaf(fmaf(acc, kTwo24 / kWScale, zv), chan, o[h]);
             }
         }
