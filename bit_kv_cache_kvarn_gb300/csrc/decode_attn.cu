@@ -42,7 +42,11 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWorkers = 2;                 // warpgroups per CTA
-constexpr int kTilesPerSplit = 16;
+constexpr int kTilesPerSplit = 16;         // one partial slot per 16-tile block of a unit (+1, below)
+constexpr int kMinPiece = 16;              // every worker's piece of the tile stream has >= 16 tiles
+constexpr int kMaxWorkers = 4096;          // plan entries reserved in the workspace
+constexpr int kIdRing = 16;                // tile-id ring of the producer
+constexpr int kIdLead = 8;                 // tile ids are fetched this many tiles ahead
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
 constexpr uint32_t kTmemCols = 256;         // worker w: A (64) and D (4 partials x 16) at 128 w
 constexpr uint32_t kBBytes = 256 * 16 * 2;  // one B operand: K = 256 x N = 16 fp16, N-contiguous
@@ -52,6 +56,14 @@ constexpr uint32_t kBKStride = 256, kBNStride = 128;  // core-matrix strides of 
 constexpr float kLazy = 4.f;
 constexpr float kWScale = 8.f;
 constexpr float kTwo24 = 16777216.f;
+
+// A worker's piece of the tile stream.  The stream lists, sequence by sequence and unit by unit
+// (unit = kv head x head block), the full tiles of each unit; a piece is a contiguous run of it.
+struct PlanEntry {
+    int b, u, j, pad;    // first tile: sequence, unit, tile within the unit
+    long long len;       // number of tiles
+    long long pad2;
+};
 
 struct DecodeArgs {
     const __nv_bfloat16* q;
@@ -69,10 +81,16 @@ struct DecodeArgs {
     const __nv_bfloat16* v_tail;
     float qscale;  // softmax scale * log2(e): scores are kept in the log2 domain
     int rotate;
-    int splits;
+    int splits;     // partial slots per (sequence, query head) = splits + 1
+    int B;
+    int units;      // units per sequence: kv heads x head blocks
+    int hblocks;    // head blocks per kv head
     float* ws;
+    long long* prefix;          // [B + 1] exclusive prefix of full tiles per sequence
+    PlanEntry* plan;            // [workers]
     float* out;
 };
+
 
 __device__ __forceinline__ int clamp_len(int len, int max_tiles) {
     const int cap = max_tiles * kTile + (kTile - 1);
@@ -266,6 +284,27 @@ __device__ __forceinline__ float warp_sum_multi(float (&v)[GH], int lane) {
     return m;
 }
 
+// Sum over the 4 warps of per-warp partials laid out [4 warps][8]: out[h] for h < GH.
+template <int GH>
+__device__ __forceinline__ void sum_warp_parts(const float* part, float (&out)[GH]) {
+    if constexpr (GH >= 4) {
+#pragma unroll
+        for (int c = 0; c < GH / 4; ++c) {
+            const float4 a = *reinterpret_cast<const float4*>(part + 4 * c);
+            const float4 b = *reinterpret_cast<const float4*>(part + 8 + 4 * c);
+            const float4 d = *reinterpret_cast<const float4*>(part + 16 + 4 * c);
+            const float4 e = *reinterpret_cast<const float4*>(part + 24 + 4 * c);
+            out[4 * c + 0] = (a.x + b.x) + (d.x + e.x);
+            out[4 * c + 1] = (a.y + b.y) + (d.y + e.y);
+            out[4 * c + 2] = (a.z + b.z) + (d.z + e.z);
+            out[4 * c + 3] = (a.w + b.w) + (d.w + e.w);
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < GH; ++h) out[h] = (part[h] + part[8 + h]) + (part[16 + h] + part[24 + h]);
+    }
+}
+
 // tcgen05.ld of NC consecutive 32-bit columns (32x32b shape; NC = 2, 4, 8 or 16).
 template <int NC>
 __device__ __forceinline__ void ld_cols(uint32_t taddr, uint32_t (&r)[NC]) {
@@ -336,29 +375,18 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
-// An item = (sequence, kv head, head block, split); items of one worker are consecutive.
-struct Item {
-    int b, kvh, hq0, split, t0, t1;
-};
-__device__ __forceinline__ Item item_at(const DecodeArgs& a, int idx, int hblocks, int gh) {
-    Item it;
-    it.split = idx % a.splits;
-    const int bhk = idx / a.splits;
-    const int hb = bhk % hblocks;
-    const int bk = bhk / hblocks;
-    it.kvh = bk % a.Hkv;
-    it.b = bk / a.Hkv;
-    it.hq0 = it.kvh * a.group + hb * gh;
-    const int n_full = clamp_len(a.seq_lens[it.b], a.max_tiles) >> 7;
-    it.t0 = it.split * kTilesPerSplit;
-    it.t1 = min(it.t0 + kTilesPerSplit, n_full);
-    if (it.t1 < it.t0) it.t1 = it.t0;
-    return it;
+__device__ __forceinline__ int full_tiles(const DecodeArgs& a, int b) {
+    return clamp_len(a.seq_lens[b], a.max_tiles) >> 7;
+}
+
+// Partial slot of (sequence b, query head hq, slot k): m, l, pad, pad, o[128].
+__device__ __forceinline__ float* slot_ptr(const DecodeArgs& a, int b, int hq, int k) {
+    return a.ws + (((size_t)b * a.Hq + hq) * (a.splits + 1) + k) * kWsStride;
 }
 
 template <int KB, int VB, int GH>
 __global__ void __launch_bounds__(kThreads, 2)
-decode_split_kernel(DecodeArgs a, int n_items) {
+decode_split_kernel(DecodeArgs a) {
     using St = Stage<KB, VB>;
     constexpr int NS = St::kCount;
     extern __shared__ __align__(1024) uint8_t dsm[];
@@ -367,7 +395,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
 
     // per-worker shared memory
     constexpr uint32_t kWorkerBytes = NS * St::kBytes + 2 * kBBytes + GH * kTile * 4 + 8 * 4 + 32 * 4 * 4 +
-                                      2 * kTilesPerSplit * 4 + 16;
+                                      kIdRing * 4 + 16;
     constexpr uint32_t kWorkerStride = (kWorkerBytes + 1023) & ~1023u;
     uint8_t* wbase = dsm + wk * kWorkerStride;
     uint8_t* bk = wbase;                                   // B operands first: 1024-byte aligned
@@ -379,17 +407,15 @@ decode_split_kernel(DecodeArgs a, int n_items) {
     float* lpart = mpart + 32;                             // [4 warps][8]
     float* zkpart = lpart + 32;                            // [4 warps][8] partial sum_j q' Z_j
     float* zvpart = zkpart + 32;                           // [4 warps][8] partial sum_t p Zv_t
-    int* tids = reinterpret_cast<int*>(zvpart + 32);       // [2][16]
+    int* idring = reinterpret_cast<int*>(zvpart + 32);     // [kIdRing] tile ids (producer)
     uint8_t* cta = dsm + kWorkers * kWorkerStride;
     uint64_t* full = reinterpret_cast<uint64_t*>(cta);     // [worker][NS]
     uint64_t* mmab = full + kWorkers * NS;                 // [worker]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmab + kWorkers);
 
-    const int hblocks = a.group / GH;
-    const int n_workers = gridDim.x * kWorkers;
+    const int hblocks = a.hblocks;
     const int worker = blockIdx.x * kWorkers + wk;
-    const int i_begin = (int)(((long long)n_items * worker) / n_workers);
-    const int i_end = (int)(((long long)n_items * (worker + 1)) / n_workers);
+    const PlanEntry piece = a.plan[worker];
 
     for (int i = tid; i < (int)(kWorkers * 2 * kBBytes / 16); i += kThreads) {
         const int wkr = i / (2 * kBBytes / 16), off = i % (2 * kBBytes / 16);
@@ -416,14 +442,42 @@ decode_split_kernel(DecodeArgs a, int n_items) {
     const uint64_t bk_desc = tc::smem_desc(bk_addr, kBKStride, kBNStride);
     const uint64_t bv_desc = tc::smem_desc(bv_addr, kBKStride, kBNStride);
 
-    // ---- producer state (thread r == 0 of the worker): tile ids of the current and next item ----
-    int p_item = i_begin, p_j = 0, p_issued = 0;  // next (item, tile) to issue; tiles issued so far
-    Item p_it;
-    auto issue = [&](int pos) {
-        // bring stream position pos into stage pos % NS
-        const int st = pos % NS;
+    // ---- producer (thread r == 0 of the worker) ----
+    // A fetch cursor walks the piece kIdLead tiles ahead of the issue cursor, bringing block-table
+    // entries into a ring with 4-byte cp.async (one commit group per tile, empty once the piece is
+    // exhausted, so a fixed wait_group depth finds the oldest id landed); the issue cursor then
+    // starts the bulk copies of that tile into its ring stage.
+    int f_b = piece.b, f_u = piece.u, f_j = piece.j, f_nt = 0;
+    long long f_left = piece.len;
+    int f_cnt = 0, i_cnt = 0;  // tile ids fetched / tiles issued
+    auto fetch_one = [&]() {
+        if (f_left > 0) {
+            const int32_t* row = a.block_table + ((size_t)f_b * a.Hkv + f_u / hblocks) * a.max_tiles;
+            cp_async4(&idring[f_cnt % kIdRing], row + f_j);
+            ++f_cnt;
+            --f_left;
+            if (++f_j == f_nt) {
+                f_j = 0;
+                if (++f_u == a.units) {
+                    f_u = 0;
+                    if (f_left > 0) {
+                        do {
+                            ++f_b;
+                            f_nt = full_tiles(a, f_b);
+                        } while (f_nt == 0);
+                    }
+                }
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto producer_issue = [&]() {
+        if (i_cnt == f_cnt) return;  // the piece is exhausted
+        fetch_one();
+        asm volatile("cp.async.wait_group %0;" ::"n"(kIdLead) : "memory");  // tile i_cnt's id is in
+        const int st = i_cnt % NS;
         uint8_t* sb = stages + st * St::kBytes;
-        const int64_t tile = tids[(p_item & 1) * kTilesPerSplit + p_j];
+        const int64_t tile = idring[i_cnt % kIdRing];
         fence_proxy_async();  // the consumers' reads of this stage come before the TMA writes
         mbar_expect_tx(&full[wk * NS + st], St::kTx);
         bulk_g2s(sb + St::kK, a.k_codes + tile * (KB * 2048), KB * 2048, &full[wk * NS + st]);
@@ -432,50 +486,34 @@ decode_split_kernel(DecodeArgs a, int n_items) {
         bulk_g2s(sb + St::kVP, a.v_params + tile * 512, 512, &full[wk * NS + st]);
         cp_async4(sb + St::kG, a.k_scale + tile);
         cp_async4_mbar(sb + St::kG + 4, a.v_scale + tile, &full[wk * NS + st]);
+        ++i_cnt;
     };
-    auto fetch_tids = [&](int item) {  // tile ids of an item into tids[item & 1] (producer only)
-        if (item >= i_end) return;
-        const Item it = item_at(a, item, hblocks, GH);
-        const int32_t* row = a.block_table + ((size_t)it.b * a.Hkv + it.kvh) * a.max_tiles;
-        for (int j = 0; j < it.t1 - it.t0; ++j) cp_async4(&tids[(item & 1) * kTilesPerSplit + j], row + it.t0 + j);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    // advance the producer to the next item with tiles; returns false at the end of the stream
-    auto producer_advance = [&]() -> bool {
-        while (p_item < i_end) {
-            if (p_j < p_it.t1 - p_it.t0) return true;
-            ++p_item;
-            p_j = 0;
-            if (p_item >= i_end) return false;
-            p_it = item_at(a, p_item, hblocks, GH);
-            asm volatile("cp.async.wait_all;" ::: "memory");  // this item's tile ids have arrived
-            fetch_tids(p_item + 1);
-        }
-        return false;
-    };
-    if (producer && i_begin < i_end) {
-        p_it = item_at(a, i_begin, hblocks, GH);
-        fetch_tids(i_begin);
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        fetch_tids(i_begin + 1);
-        for (int s = 0; s < NS; ++s) {
-            if (!producer_advance()) break;
-            issue(p_issued);
-            ++p_issued;
-            ++p_j;
-        }
+    if (producer && piece.len > 0) {
+        f_nt = full_tiles(a, f_b);
+        for (int k = 0; k < kIdLead; ++k) fetch_one();
+        for (int k = 0; k < NS; ++k) producer_issue();
     }
 
     uint32_t mma_phase = 0;
     int pos = 0;       // consumer stream position
+    int c_st = 0;      // its ring stage (pos % NS) and phase parity ((pos / NS) & 1)
+    uint32_t c_ph = 0;
     bool ok = true;    // this thread's waits all succeeded
     bool alive = true;  // uniform over the worker: changes only at AND-barriers
-    for (int item = i_begin; item < i_end && alive; ++item) {
-        const Item it = item_at(a, item, hblocks, GH);
-        const int n_t = it.t1 - it.t0;
-        // rotated queries of this item's heads, scaled so |q'| 2^E <= 2^7 (q' S1 <= 2^15 in fp16)
+    // consumer cursor over the piece: unit (cb, cu) from tile cj, c_left tiles to go
+    int cb = piece.b, cu = piece.u, cj = piece.j;
+    long long c_left = piece.len;
+    int c_nt = c_left > 0 ? full_tiles(a, cb) : 0;
+    bool cont = false;  // the current unit was entered from the previous one (not at the piece start)
+    while (c_left > 0 && alive) {
+        // one segment: the tiles of unit (cb, cu) from cj on that belong to this piece
+        const int kvh = cu / hblocks, hb = cu % hblocks;
+        const int hq0 = kvh * a.group + hb * GH;
+        const int seg_j0 = cj;
+        const int n_t = (int)min((long long)(c_nt - cj), c_left);
+        // rotated queries of the unit's heads, scaled so |q'| 2^E <= 2^7 (q' S1 <= 2^15 in fp16)
         for (int h = wq; h < GH; h += 4) {
-            const __nv_bfloat16* qp = a.q + ((size_t)it.b * a.Hq + it.hq0 + h) * kTile + 4 * lane;
+            const __nv_bfloat16* qp = a.q + ((size_t)cb * a.Hq + hq0 + h) * kTile + 4 * lane;
             const uint2 raw = *reinterpret_cast<const uint2*>(qp);
             const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
             const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
@@ -501,16 +539,26 @@ decode_split_kernel(DecodeArgs a, int n_items) {
         named_sync(bar_id, 128);
 
         float m_run[GH], l_part[GH], o[GH];
+        // the item's rotated query for channel r and its scale, kept in registers for small groups
+        constexpr bool kQReg = GH <= 4;
+        float qreg[kQReg ? GH : 1], ereg[kQReg ? GH : 1];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             m_run[h] = -INFINITY;
             l_part[h] = 0.f;
             o[h] = 0.f;
+            if constexpr (kQReg) {
+                qreg[h] = qrs[h * kTile + r];
+                ereg[h] = einv[h];
+            }
         }
         for (int j = 0; j < n_t && alive; ++j, ++pos) {
-            const int st = pos % NS;
-            const uint8_t* sb = stages + st * St::kBytes;
-            ok = mbar_wait(&full[wk * NS + st], (pos / NS) & 1, &g_decode_error) && ok;
+            const uint8_t* sb = stages + c_st * St::kBytes;
+            ok = mbar_wait(&full[wk * NS + c_st], c_ph, &g_decode_error) && ok;
+            if (++c_st == NS) {
+                c_st = 0;
+                c_ph ^= 1u;
+            }
             const float* qv = qrs;
 
             // ---- scores: A = K codes of token r, B = q' S1 2^-shift of channel r ----
@@ -527,7 +575,9 @@ decode_split_kernel(DecodeArgs a, int n_items) {
                 const float z = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kKP + 256)[r]);
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    const float q = qv[h * kTile + r];
+                    float q;
+                    if constexpr (kQReg) q = qreg[h];
+                    else q = qv[h * kTile + r];
                     xs[h] = q * s1;
                     xz[h] = q * z;
                 }
@@ -558,11 +608,7 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             if (producer) {
                 // while the MMAs run: refill the stage the previous tile used (every thread of the
                 // worker is past it: they all reached the barrier above)
-                if (pos > 0 && alive && producer_advance()) {
-                    issue(p_issued);
-                    ++p_issued;
-                    ++p_j;
-                }
+                if (pos > 0 && alive) producer_issue();
             }
             ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
@@ -575,14 +621,18 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             // exceeds it by more than kLazy (p <= 2^kLazy keeps p S1 kWScale inside fp16); otherwise
             // (always on an item's first tile) the tile maximum is taken exactly and the partial
             // sums are rescaled.
-            float sc[GH], p[GH];
+            float sc[GH], p[GH], zks[GH];
             const float tok = gk * e4m3_value(sb[St::kKP + 128 + r]);
             bool over = false;
+            sum_warp_parts<GH>(zkpart, zks);
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
-                const float zk = (zkpart[h] + zkpart[8 + h]) + (zkpart[16 + h] + zkpart[24 + h]);
+                const float zk = zks[h];
                 const float dot = dsum[2 * h] + dsum[2 * h + 1];
-                sc[h] = fmaf(dot, einv[h], zk * (einv[h] * (1.f / kTwo24))) * tok;
+                float ei;
+                if constexpr (kQReg) ei = ereg[h];
+                else ei = einv[h];
+                sc[h] = fmaf(dot, ei, zk * (ei * (1.f / kTwo24))) * tok;
                 over = over || !(sc[h] <= m_run[h] + kLazy);
                 p[h] = exp2f(sc[h] - m_run[h]);
             }
@@ -659,41 +709,153 @@ decode_split_kernel(DecodeArgs a, int n_items) {
             mma_phase ^= 1;
             tc::fence_after();
             read_partials<GH>(d_col + lane_off, dsum);
+            float zvs[GH];
+            sum_warp_parts<GH>(zvpart, zvs);
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
-                const float zv = (zvpart[h] + zvpart[8 + h]) + (zvpart[16 + h] + zvpart[24 + h]);
+                const float zv = zvs[h];
                 const float acc = dsum[2 * h] + dsum[2 * h + 1];
                 o[h] = fmaf(fmaf(acc, kTwo24 / kWScale, zv), chan, o[h]);
             }
         }
 
-        // ---- this item's partial (m, l, o) for its heads ----
+        // ---- this segment's partial (m, l, o) for its heads ----
+        // Slots of a unit: k < ceil(nt / 16) for the 16-tile block in which a piece starts, and
+        // slot `splits` for the piece that enters the unit from the previous one.  As every piece
+        // has >= 16 tiles, no two pieces start in one block; blocks that no piece starts in lie
+        // wholly inside one segment, which marks their slots empty -- so every slot the merge
+        // reads is written exactly once.
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             const float ls = warp_sum(l_part[h]);
             if (lane == 0) lpart[wq * 8 + h] = ls;
         }
         alive = named_sync_and(bar_id, 128, ok && alive);
+        {
+            const int seg_j1 = seg_j0 + n_t;
+            const int own = cont ? a.splits : seg_j0 / kTilesPerSplit;
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            float* dst = a.ws + (((size_t)it.b * a.Hq + it.hq0 + h) * a.splits + it.split) * kWsStride;
-            dst[4 + r] = o[h];
-            if (r == 0) {
-                dst[0] = m_run[h];
-                dst[1] = lpart[h] + lpart[8 + h] + lpart[16 + h] + lpart[24 + h];
+            for (int h = 0; h < GH; ++h) {
+                float* dst = slot_ptr(a, cb, hq0 + h, own);
+                dst[4 + r] = o[h];
+                if (r == 0) {
+                    dst[0] = m_run[h];
+                    dst[1] = lpart[h] + lpart[8 + h] + lpart[16 + h] + lpart[24 + h];
+                }
+            }
+            const int n_blk = (c_nt + kTilesPerSplit - 1) / kTilesPerSplit;
+            for (int k = r; k < n_blk; k += 128) {
+                const int k0 = k * kTilesPerSplit, k1 = min(k0 + kTilesPerSplit, c_nt);
+                if (k != own && k0 >= seg_j0 && k1 <= seg_j1) {
+#pragma unroll
+                    for (int h = 0; h < GH; ++h) {
+                        float* dst = slot_ptr(a, cb, hq0 + h, k);
+                        dst[0] = -INFINITY;
+                        dst[1] = 0.f;
+                    }
+                }
+            }
+            if (!cont && seg_j0 == 0 && r == 0) {
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    float* dst = slot_ptr(a, cb, hq0 + h, a.splits);
+                    dst[0] = -INFINITY;
+                    dst[1] = 0.f;
+                }
             }
         }
-        named_sync(bar_id, 128);  // lpart / qrs are rewritten by the next item
+        named_sync(bar_id, 128);  // lpart / qrs are rewritten by the next segment
+        // advance the cursor to the next unit with full tiles
+        c_left -= n_t;
+        cj = 0;
+        cont = true;
+        if (++cu == a.units) {
+            cu = 0;
+            if (c_left > 0) {
+                do {
+                    ++cb;
+                    c_nt = full_tiles(a, cb);
+                } while (c_nt == 0);
+            }
+        }
     }
     if (producer) {
         // after a give-up, wait (bounded) for copies still in flight before the CTA exits
-        for (int q = pos; q < p_issued; ++q) mbar_drain(&full[wk * NS + q % NS], (q / NS) & 1);
+        for (int q = pos; q < i_cnt; ++q) mbar_drain(&full[wk * NS + q % NS], (q / NS) & 1);
         asm volatile("cp.async.wait_all;" ::: "memory");
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     if (warp == 0) tc::dealloc(tmem, kTmemCols);
+}
+
+// One block of 1024 threads: prefix sums of the full tiles per sequence, then each worker's piece
+// of the tile stream -- equal shares of >= kMinPiece tiles, so the split kernel is balanced to a
+// tile whatever the length mix.
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a, int n_workers) {
+    __shared__ long long warp_tot[32];
+    __shared__ long long carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < a.B; base += 1024) {
+        const int b = base + tid;
+        const long long v = b < a.B ? (long long)full_tiles(a, b) : 0;
+        long long inc = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += y;
+        }
+        if (lane == 31) warp_tot[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            long long t = warp_tot[lane], ti = t;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, ti, d);
+                if (lane >= d) ti += y;
+            }
+            warp_tot[lane] = ti - t;  // exclusive prefix of the warp totals
+        }
+        __syncthreads();
+        const long long c0 = carry;
+        if (b < a.B) a.prefix[b] = c0 + warp_tot[warp] + inc - v;
+        __syncthreads();
+        if (tid == 1023) carry = c0 + warp_tot[31] + inc;
+        __syncthreads();
+    }
+    if (tid == 0) a.prefix[a.B] = carry;
+    __syncthreads();
+    const long long units = a.units;
+    const long long total = units * carry;
+    long long w_used = total / kMinPiece;
+    if (w_used < 1) w_used = total > 0 ? 1 : 0;
+    if (w_used > n_workers) w_used = n_workers;
+    for (int w = tid; w < n_workers; w += 1024) {
+        PlanEntry e;
+        e.b = e.u = e.j = e.pad = 0;
+        e.len = 0;
+        e.pad2 = 0;
+        if (w < w_used) {
+            const long long g0 = total * w / w_used, g1 = total * (w + 1) / w_used;
+            // last sequence whose first tile is at or before g0 (it has full tiles)
+            int lo = 0, hi = a.B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (units * a.prefix[mid] <= g0) lo = mid;
+                else hi = mid - 1;
+            }
+            const long long rem = g0 - units * a.prefix[lo];
+            const long long nt = a.prefix[lo + 1] - a.prefix[lo];
+            e.b = lo;
+            e.u = (int)(rem / nt);
+            e.j = (int)(rem % nt);
+            e.len = g1 - g0;
+        }
+        a.plan[w] = e;
+    }
 }
 
 // One warp per (sequence, query head): merge splits, inverse rotation, bf16 tail, normalise.
@@ -703,15 +865,21 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     const int kvh = hq / a.group;
     const int len = clamp_len(a.seq_lens[b], a.max_tiles);
     const int tail = len & 127;
-    const float* base = a.ws + ((size_t)b * a.Hq + hq) * a.splits * kWsStride;
+    const int nt = len >> 7;
+    const float* base = slot_ptr(a, b, hq, 0);
+    // the slots this (sequence, head) has: one per 16-tile block and the unit-entry slot
+    const int n_slots = nt > 0 ? (nt + kTilesPerSplit - 1) / kTilesPerSplit + 1 : 0;
+    auto slot_of = [&](int i) { return i + 1 == n_slots ? a.splits : i; };
 
     float mmax = -INFINITY;
-    for (int s = lane; s < a.splits; s += 32) mmax = fmaxf(mmax, base[s * kWsStride]);
+    for (int i = lane; i < n_slots; i += 32) mmax = fmaxf(mmax, base[slot_of(i) * kWsStride]);
     mmax = warp_max(mmax);
     float l = 0.f;
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     if (mmax != -INFINITY) {
-        for (int s = 0; s < a.splits; ++s) {
+        for (int i = 0; i < n_slots; ++i) {
+            const int s = slot_of(i);
+            if (base[s * kWsStride] == -INFINITY) continue;  // an empty slot (o is not written)
             const float f = exp2f(base[s * kWsStride] - mmax);
             l = fmaf(base[s * kWsStride + 1], f, l);
             const float4 v = *reinterpret_cast<const float4*>(base + s * kWsStride + 4 + 4 * lane);
@@ -757,45 +925,52 @@ template <int KB, int VB, int GH>
 size_t split_smem_bytes() {
     using St = Stage<KB, VB>;
     constexpr uint32_t kWorkerBytes = St::kCount * St::kBytes + 2 * kBBytes + GH * kTile * 4 + 8 * 4 + 32 * 4 * 4 +
-                                      2 * kTilesPerSplit * 4 + 16;
+                                      kIdRing * 4 + 16;
     constexpr uint32_t kWorkerStride = (kWorkerBytes + 1023) & ~1023u;
     size_t bytes = (size_t)kWorkers * kWorkerStride + kWorkers * St::kCount * 8 + kWorkers * 8 + 16;
     // at least 80 KB, so no more than two CTAs (2 x 256 TMEM columns) share an SM
     return bytes < 80 * 1024 ? 80 * 1024 : bytes;
 }
 
+int split_grid() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    int grid = 2 * sms;  // persistent: two CTAs per SM
+    if (grid * kWorkers > kMaxWorkers) grid = kMaxWorkers / kWorkers;
+    return grid;
+}
+
 template <int KB, int VB, int GH>
-cudaError_t run_split(const DecodeArgs& a, int n_items, cudaStream_t stream) {
+cudaError_t run_split(const DecodeArgs& a, int grid, cudaStream_t stream) {
     auto kern = decode_split_kernel<KB, VB, GH>;
     const size_t smem = split_smem_bytes<KB, VB, GH>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    const int want = (n_items + kWorkers - 1) / kWorkers;
-    const int grid = want < 2 * sms ? want : 2 * sms;  // persistent: two CTAs per SM
-    kern<<<grid, kThreads, smem, stream>>>(a, n_items);
+    kern<<<grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <int KB, int VB>
-cudaError_t run_split_g(const DecodeArgs& a, int gh, int n_items, cudaStream_t stream) {
-    if (gh == 1) return run_split<KB, VB, 1>(a, n_items, stream);
-    if (gh == 2) return run_split<KB, VB, 2>(a, n_items, stream);
-    if (gh == 4) return run_split<KB, VB, 4>(a, n_items, stream);
-    return run_split<KB, VB, 8>(a, n_items, stream);
+cudaError_t run_split_g(const DecodeArgs& a, int gh, int grid, cudaStream_t stream) {
+    if (gh == 1) return run_split<KB, VB, 1>(a, grid, stream);
+    if (gh == 2) return run_split<KB, VB, 2>(a, grid, stream);
+    if (gh == 4) return run_split<KB, VB, 4>(a, grid, stream);
+    return run_split<KB, VB, 8>(a, grid, stream);
 }
 
 }  // namespace
 
+// Workspace: partial slots [B][Hq][splits + 1][132] f32 | prefix [B + 1] i64 | plan [4096] x 32 B,
+// each part 256-byte aligned.
 DecodePlan plan_decode(int B, int Hq, int /*Hkv*/, int max_tiles) {
     DecodePlan p;
     p.tiles_per_split = kTilesPerSplit;
     p.splits = max_tiles <= 0 ? 1 : (max_tiles + kTilesPerSplit - 1) / kTilesPerSplit;
-    p.workspace_bytes = (size_t)B * Hq * p.splits * kWsStride * sizeof(float);
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    p.prefix_offset = up((size_t)B * Hq * (p.splits + 1) * kWsStride * sizeof(float));
+    p.plan_offset = p.prefix_offset + up((size_t)(B + 1) * sizeof(long long));
+    p.workspace_bytes = p.plan_offset + (size_t)kMaxWorkers * sizeof(PlanEntry);
     return p;
 }
 
@@ -834,15 +1009,23 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.qscale = softmax_scale * kLog2e;
     a.rotate = rotate;
     a.splits = plan.splits;
-    a.ws = static_cast<float*>(workspace);
-    a.out = out;
+    a.B = B;
     const int gh = group;  // up to 8 heads x (hi, lo) fill the 16 MMA columns
-    const int n_items = B * Hkv * (group / gh) * plan.splits;
-    cudaError_t e;
-    if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, n_items, stream);
-    else if (k_bits == 4 && v_bits == 2) e = run_split_g<4, 2>(a, gh, n_items, stream);
-    else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, n_items, stream);
-    else e = run_split_g<4, 4>(a, gh, n_items, stream);
+    a.hblocks = group / gh;
+    a.units = Hkv * a.hblocks;
+    a.ws = static_cast<float*>(workspace);
+    a.prefix = reinterpret_cast<long long*>(static_cast<uint8_t*>(workspace) + plan.prefix_offset);
+    a.plan = reinterpret_cast<PlanEntry*>(static_cast<uint8_t*>(workspace) + plan.plan_offset);
+    a.out = out;
+    const int grid = split_grid();
+    if (grid <= 0) return cudaErrorInvalidDevice;
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a, grid * kWorkers);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, grid, stream);
+    else if (k_bits == 4 && v_bits == 2) e = run_split_g<4, 2>(a, gh, grid, stream);
+    else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, grid, stream);
+    else e = run_split_g<4, 4>(a, gh, grid, stream);
     if (e != cudaSuccess) return e;
     decode_merge_kernel<<<dim3(Hq, B), 32, 0, stream>>>(a);
     return cudaGetLastError();

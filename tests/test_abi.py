@@ -123,8 +123,15 @@ def test_workspace_plan(lib):
     import bit_kv_cache_kvarn_gb300 as kv
 
     cfg = _cfg()
-    # 16 tiles per split; (m, l, 2 pad, o[128]) floats per (sequence, query head, split)
-    assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == 16 * 32 * 16 * 132 * 4
-    assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == 4 * 40 * 64 * 132 * 4
-    assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == 1 * 4 * 1 * 132 * 4
+
+    def expected(B, Hq, max_tiles):
+        # partial slots: one per 16-tile block plus one; (m, l, 2 pad, o[128]) floats per slot;
+        # then int64 prefix sums [B + 1] and 4096 work descriptors of 32 bytes, 256-byte aligned
+        up = lambda x: (x + 255) // 256 * 256
+        slots = max(1, -(-max_tiles // 16)) + 1
+        return up(B * Hq * slots * 132 * 4) + up((B + 1) * 8) + 4096 * 32
+
+    assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == expected(16, 32, 256)
+    assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == expected(4, 40, 1024)
+    assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == expected(1, 4, 0)
     assert kv.kvarn_decode_workspace_size(cfg, 1, 6, 4, 1) == 0
