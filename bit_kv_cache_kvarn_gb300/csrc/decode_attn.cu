@@ -45,8 +45,8 @@ constexpr int kWorkers = 2;                 // warpgroups per CTA
 constexpr int kTilesPerSplit = 16;         // one partial slot per 16-tile block of a unit (+1, below)
 constexpr int kMinPiece = 16;              // every worker's piece of the tile stream has >= 16 tiles
 constexpr int kMaxWorkers = 4096;          // plan entries reserved in the workspace
-constexpr int kIdRing = 16;                // tile-id ring of the producer
-constexpr int kIdLead = 8;                 // tile ids are fetched this many tiles ahead
+constexpr int kIdRing = 32;                // tile-id ring of a worker
+constexpr int kIdBatch = 16;               // tile ids are fetched 16 at a time, one batch ahead
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
 constexpr uint32_t kTmemCols = 256;         // worker w: A (64) and D (4 partials x 16) at 128 w
 constexpr uint32_t kBBytes = 256 * 16 * 2;  // one B operand: K = 256 x N = 16 fp16, N-contiguous
@@ -97,16 +97,14 @@ __device__ __forceinline__ int clamp_len(int len, int max_tiles) {
     return len < 0 ? 0 : (len > cap ? cap : len);
 }
 
-// Shared-memory ring stage: K codes | V codes | K params | V params | g_K, g_V.
+// Shared-memory ring stage: K codes | V codes | K params | V params, one bulk copy each.
 template <int KB, int VB>
 struct Stage {
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = KB * 2048;
     static constexpr uint32_t kKP = kV + VB * 2048;
     static constexpr uint32_t kVP = kKP + 512;
-    static constexpr uint32_t kG = kVP + 512;
-    static constexpr uint32_t kBytes = kG + 16;
-    static constexpr uint32_t kTx = kG;  // bytes delivered by the bulk copies
+    static constexpr uint32_t kBytes = kVP + 512;
     static constexpr int kCount = (KB + VB == 4) ? 3 : 2;
 };
 
@@ -365,16 +363,6 @@ __device__ __forceinline__ bool named_sync_and(int id, int n, bool flag) {
     return out != 0;
 }
 
-// 4-byte asynchronous global -> shared copy, tracked by an mbarrier (which then expects one more
-// arrival from this thread).
-__device__ __forceinline__ void cp_async4_mbar(void* dst, const void* src, uint64_t* bar) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-
 __device__ __forceinline__ int full_tiles(const DecodeArgs& a, int b) {
     return clamp_len(a.seq_lens[b], a.max_tiles) >> 7;
 }
@@ -421,7 +409,7 @@ decode_split_kernel(DecodeArgs a) {
         const int wkr = i / (2 * kBBytes / 16), off = i % (2 * kBBytes / 16);
         reinterpret_cast<uint4*>(dsm + wkr * kWorkerStride)[off] = make_uint4(0, 0, 0, 0);
     }
-    if (tid < kWorkers * NS) mbar_init(&full[tid], 2);  // the bulk-copy arrival + the cp.async arrival
+    if (tid < kWorkers * NS) mbar_init(&full[tid], 4);  // one arrival per copy (one per warp)
     if (tid < kWorkers) mbar_init(&mmab[tid], 4);  // one tcgen05.commit per warp of the worker
     if (warp == 0) tc::alloc(tmem_slot, kTmemCols);
     fence_mbar_init();
@@ -442,56 +430,81 @@ decode_split_kernel(DecodeArgs a) {
     const uint64_t bk_desc = tc::smem_desc(bk_addr, kBKStride, kBNStride);
     const uint64_t bv_desc = tc::smem_desc(bv_addr, kBKStride, kBNStride);
 
-    // ---- producer (thread r == 0 of the worker) ----
-    // A fetch cursor walks the piece kIdLead tiles ahead of the issue cursor, bringing block-table
-    // entries into a ring with 4-byte cp.async (one commit group per tile, empty once the piece is
-    // exhausted, so a fixed wait_group depth finds the oldest id landed); the issue cursor then
-    // starts the bulk copies of that tile into its ring stage.
-    int f_b = piece.b, f_u = piece.u, f_j = piece.j, f_nt = 0;
-    long long f_left = piece.len;
-    int f_cnt = 0, i_cnt = 0;  // tile ids fetched / tiles issued
-    auto fetch_one = [&]() {
-        if (f_left > 0) {
-            const int32_t* row = a.block_table + ((size_t)f_b * a.Hkv + f_u / hblocks) * a.max_tiles;
-            cp_async4(&idring[f_cnt % kIdRing], row + f_j);
-            ++f_cnt;
-            --f_left;
-            if (++f_j == f_nt) {
-                f_j = 0;
-                if (++f_u == a.units) {
-                    f_u = 0;
-                    if (f_left > 0) {
-                        do {
-                            ++f_b;
-                            f_nt = full_tiles(a, f_b);
-                        } while (f_nt == 0);
-                    }
-                }
+    // ---- tile ids and copies ----
+    // Warp 0 keeps the block-table entries of the coming 16..32 tiles of the piece in a 32-entry
+    // ring in shared memory: the first 32 are loaded at the start; at every 16th tile the batch
+    // loaded 16 tiles earlier (plain loads into registers) is stored and the next one is loaded.  The four
+    // bulk copies of a tile (K codes, V codes, K params, V params) are issued by lane 0 of the
+    // four warps, each arriving on the stage barrier with its own byte count: an issue blocks its
+    // thread for ~100 cycles, so the copies are spread instead of serialised in one thread.
+    int f_b = piece.b, f_u = piece.u, f_j = piece.j, f_nt = 0;  // first tile of the next batch
+    long long f_left = piece.len;                                // tiles not yet fetched
+    int f_pos = 0;                                               // stream position of that tile
+    int pend_id = 0, pend_n = 0, pend_pos = 0;                   // a loaded, not yet stored batch
+    // advance (b, u, j) of this piece's stream by n tiles (n >= 0)
+    auto advance = [&](int& b, int& u, int& j, int& nt, int n) {
+        j += n;
+        while (j >= nt) {
+            j -= nt;
+            if (++u == a.units) {
+                u = 0;
+                do {
+                    ++b;
+                    nt = full_tiles(a, b);
+                } while (nt == 0);
             }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    auto producer_issue = [&]() {
-        if (i_cnt == f_cnt) return;  // the piece is exhausted
-        fetch_one();
-        asm volatile("cp.async.wait_group %0;" ::"n"(kIdLead) : "memory");  // tile i_cnt's id is in
-        const int st = i_cnt % NS;
+    auto fetch_batch = [&](int width) {  // warp 0: load the ids of the next `width` tiles
+        const int n = (int)min((long long)width, f_left);
+        pend_n = n;
+        pend_pos = f_pos;
+        if (lane < n) {
+            int b = f_b, u = f_u, j = f_j, nt = f_nt;
+            advance(b, u, j, nt, lane);
+            pend_id = a.block_table[((size_t)b * a.Hkv + u / hblocks) * a.max_tiles + j];
+        }
+        f_left -= n;
+        f_pos += n;
+        if (f_left > 0) advance(f_b, f_u, f_j, f_nt, n);
+    };
+    auto store_batch = [&]() {  // warp 0: the loaded ids into the ring
+        if (lane < pend_n) idring[(pend_pos + lane) % kIdRing] = pend_id;
+        pend_n = 0;
+    };
+    // copies of stream position i into its stage; every warp's lane 0 calls this for the same i
+    auto issue_copies = [&](int i) {
+        if (lane != 0) return;
+        const int st = i % NS;
         uint8_t* sb = stages + st * St::kBytes;
-        const int64_t tile = idring[i_cnt % kIdRing];
+        uint64_t* bar = &full[wk * NS + st];
+        const int64_t tile = idring[i % kIdRing];
         fence_proxy_async();  // the consumers' reads of this stage come before the TMA writes
-        mbar_expect_tx(&full[wk * NS + st], St::kTx);
-        bulk_g2s(sb + St::kK, a.k_codes + tile * (KB * 2048), KB * 2048, &full[wk * NS + st]);
-        bulk_g2s(sb + St::kV, a.v_codes + tile * (VB * 2048), VB * 2048, &full[wk * NS + st]);
-        bulk_g2s(sb + St::kKP, a.k_params + tile * 512, 512, &full[wk * NS + st]);
-        bulk_g2s(sb + St::kVP, a.v_params + tile * 512, 512, &full[wk * NS + st]);
-        cp_async4(sb + St::kG, a.k_scale + tile);
-        cp_async4_mbar(sb + St::kG + 4, a.v_scale + tile, &full[wk * NS + st]);
-        ++i_cnt;
+        if (wq == 0) {
+            mbar_expect_tx(bar, KB * 2048);
+            bulk_g2s(sb + St::kK, a.k_codes + tile * (KB * 2048), KB * 2048, bar);
+        } else if (wq == 1) {
+            mbar_expect_tx(bar, VB * 2048);
+            bulk_g2s(sb + St::kV, a.v_codes + tile * (VB * 2048), VB * 2048, bar);
+        } else if (wq == 2) {
+            mbar_expect_tx(bar, 512);
+            bulk_g2s(sb + St::kKP, a.k_params + tile * 512, 512, bar);
+        } else {
+            mbar_expect_tx(bar, 512);
+            bulk_g2s(sb + St::kVP, a.v_params + tile * 512, 512, bar);
+        }
     };
-    if (producer && piece.len > 0) {
-        f_nt = full_tiles(a, f_b);
-        for (int k = 0; k < kIdLead; ++k) fetch_one();
-        for (int k = 0; k < NS; ++k) producer_issue();
+    int issued = 0;  // stream positions whose copies are issued (uniform over the worker)
+    if (piece.len > 0) {
+        if (wq == 0) {
+            f_nt = full_tiles(a, f_b);
+            fetch_batch(kIdRing);
+            store_batch();
+            if (f_left > 0) fetch_batch(kIdBatch);
+        }
+        named_sync(bar_id, 128);  // the first batch of ids is in the ring
+        issued = (int)min((long long)NS, piece.len);
+        for (int i = 0; i < issued; ++i) issue_copies(i);
     }
 
     uint32_t mma_phase = 0;
@@ -554,6 +567,17 @@ decode_split_kernel(DecodeArgs a) {
         }
         for (int j = 0; j < n_t && alive; ++j, ++pos) {
             const uint8_t* sb = stages + c_st * St::kBytes;
+            // tile factors by plain loads: they arrive long before the softmax needs them
+            const int64_t tile_id = idring[pos % kIdRing];
+            const float gk = __ldg(a.k_scale + tile_id);
+            const float gv = __ldg(a.v_scale + tile_id);
+            if (wq == 0 && (pos % kIdBatch) == 0 && pos > 0) {
+                // the batch loaded 16 tiles ago (positions pos + 16 .. pos + 31) goes into the
+                // slots of positions pos - 16 .. pos - 1, all read before this tile's barriers;
+                // its first reader is the refill at pos + 14, after this tile's barrier
+                store_batch();
+                if (f_left > 0) fetch_batch(kIdBatch);
+            }
             ok = mbar_wait(&full[wk * NS + c_st], c_ph, &g_decode_error) && ok;
             if (++c_st == NS) {
                 c_st = 0;
@@ -567,8 +591,6 @@ decode_split_kernel(DecodeArgs a) {
                 load_row<KB>(sb + St::kK, r, x);
                 unpack_row_to_tmem<KB>(x, a_col + lane_off);
             }
-            const float gk = *reinterpret_cast<const float*>(sb + St::kG);
-            const float gv = *reinterpret_cast<const float*>(sb + St::kG + 4);
             {
                 float xs[GH], xz[GH];
                 const float s1 = e4m3_value(sb[St::kKP + r]) * pre_k;
@@ -605,10 +627,11 @@ decode_split_kernel(DecodeArgs a) {
                 }
                 tc::commit(&mmab[wk]);
             }
-            if (producer) {
-                // while the MMAs run: refill the stage the previous tile used (every thread of the
-                // worker is past it: they all reached the barrier above)
-                if (pos > 0 && alive) producer_issue();
+            // while the MMAs run: refill the stage the previous tile used (every thread of the
+            // worker is past it: they all reached the barrier above)
+            if (pos > 0 && issued < piece.len) {
+                issue_copies(issued);
+                ++issued;
             }
             ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
@@ -781,8 +804,7 @@ decode_split_kernel(DecodeArgs a) {
     }
     if (producer) {
         // after a give-up, wait (bounded) for copies still in flight before the CTA exits
-        for (int q = pos; q < i_cnt; ++q) mbar_drain(&full[wk * NS + q % NS], (q / NS) & 1);
-        asm volatile("cp.async.wait_all;" ::: "memory");
+        for (int q = pos; q < issued; ++q) mbar_drain(&full[wk * NS + q % NS], (q / NS) & 1);
     }
     tc::fence_before();
     __syncthreads();
