@@ -51,6 +51,8 @@ _SIGNATURES = {
     "kvarn_tile_code_bytes": (_sz, [_i32]),
     "kvarn_tile_param_bytes": (_sz, []),
     "kvarn_encode_blocks": (_i32, [ctypes.POINTER(kvarn_config), _i32, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "kvarn_encode_kv_blocks": (_i32, [ctypes.POINTER(kvarn_config), _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp]),
     "kvarn_dequant": (_i32, [ctypes.POINTER(kvarn_config), _i32, _vp, _vp, _vp, _i64, _i32, _vp, _vp]),
     "kvarn_decode_workspace_size": (_sz, [ctypes.POINTER(kvarn_config), _i32, _i32, _i32, _i32]),
     "kvarn_decode_attention": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
@@ -147,6 +149,25 @@ def kvarn_encode_blocks(cfg: kvarn_config, kind: int, x, codes, params, tile_sca
     _need(tile_scale, torch.float32, n_tiles, "tile_scale")
     _check(load().kvarn_encode_blocks(ctypes.byref(cfg), kind, _ptr(x), n_tiles, _ptr(codes),
                                       _ptr(params), _ptr(tile_scale), _stream(stream)))
+
+
+def kvarn_encode_kv_blocks(cfg: kvarn_config, k, v, k_codes, k_params, k_scale, v_codes, v_params,
+                           v_scale, stream=None, n_tiles: int | None = None):
+    """K and V blocks [n, 128, 128] bf16 encoded in one launch (same results as two
+    kvarn_encode_blocks calls)."""
+    if n_tiles is None:
+        n_tiles = k.shape[0]
+    for x, name in ((k, "k"), (v, "v")):
+        _need(x, torch.bfloat16, n_tiles * TILE * TILE, name)
+    _need(k_codes, torch.uint8, n_tiles * TILE * 16 * cfg.k_bits, "k_codes")
+    _need(v_codes, torch.uint8, n_tiles * TILE * 16 * cfg.v_bits, "v_codes")
+    for t, name in ((k_params, "k_params"), (v_params, "v_params")):
+        _need(t, torch.uint8, n_tiles * PARAM_BYTES, name)
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, torch.float32, n_tiles, name)
+    _check(load().kvarn_encode_kv_blocks(ctypes.byref(cfg), _ptr(k), _ptr(v), n_tiles, _ptr(k_codes),
+                                         _ptr(k_params), _ptr(k_scale), _ptr(v_codes), _ptr(v_params),
+                                         _ptr(v_scale), _stream(stream)))
 
 
 def kvarn_dequant(cfg: kvarn_config, kind: int, codes, params, tile_scale, out, original_basis=1,

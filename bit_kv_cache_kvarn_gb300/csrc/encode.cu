@@ -509,4 +509,21 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
     return run(encode_kernel<4, KVARN_KIND_V>);
 }
 
+// K then V blocks of one call: two launches in stream order.  (Overlapping the two grids -- one
+// fused grid, or the V grid started early on the SMs the K grid leaves -- measured slower when the
+// inputs come from HBM rather than L2, so they run one after the other.)
+cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_k, void* k_codes,
+                             void* k_params, float* k_scale, const void* v_x, int64_t n_v, void* v_codes,
+                             void* v_params, float* v_scale, int iters, int rotate, int normalize,
+                             cudaStream_t stream) {
+    if (n_k > 0) {
+        cudaError_t e = launch_encode(k_bits, KVARN_KIND_K, k_x, n_k, k_codes, k_params, k_scale, iters, rotate,
+                                      normalize, stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (n_v == 0) return cudaSuccess;
+    return launch_encode(v_bits, KVARN_KIND_V, v_x, n_v, v_codes, v_params, v_scale, iters, rotate, normalize,
+                         stream);
+}
+
 }  // namespace kvarn

@@ -105,6 +105,29 @@ kvarn_status kvarn_encode_blocks(const kvarn_config* cfg, kvarn_kind kind, const
     return ok();
 }
 
+kvarn_status kvarn_encode_kv_blocks(const kvarn_config* cfg, const void* k_bf16, const void* v_bf16,
+                                    int64_t n_tiles, void* k_codes, void* k_params, float* k_scale,
+                                    void* v_codes, void* v_params, float* v_scale,
+                                    kvarn_stream_t stream) {
+    KV_TRY(check_cfg(cfg));
+    if (n_tiles < 0) return fail(KVARN_ERR_INVALID_ARG, "n_tiles = %lld < 0", (long long)n_tiles);
+    if (n_tiles == 0) return ok();
+    KV_TRY(check_ptr(k_bf16, 16, "k_bf16"));
+    KV_TRY(check_ptr(v_bf16, 16, "v_bf16"));
+    KV_TRY(check_ptr(k_codes, 16, "k_codes"));
+    KV_TRY(check_ptr(k_params, 16, "k_params"));
+    KV_TRY(check_ptr(k_scale, 4, "k_scale"));
+    KV_TRY(check_ptr(v_codes, 16, "v_codes"));
+    KV_TRY(check_ptr(v_params, 16, "v_params"));
+    KV_TRY(check_ptr(v_scale, 4, "v_scale"));
+    cudaError_t e = kvarn::launch_encode_kv(cfg->k_bits, cfg->v_bits, k_bf16, n_tiles, k_codes, k_params,
+                                            k_scale, v_bf16, n_tiles, v_codes, v_params, v_scale,
+                                            cfg->sinkhorn_iters, !(cfg->flags & KVARN_FLAG_NO_ROTATE),
+                                            !(cfg->flags & KVARN_FLAG_NO_NORMALIZE), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "encode launch");
+    return ok();
+}
+
 kvarn_status kvarn_dequant(const kvarn_config* cfg, kvarn_kind kind, const void* codes,
                            const void* params, const float* tile_scale, int64_t n_tiles,
                            int original_basis, float* out, kvarn_stream_t stream) {

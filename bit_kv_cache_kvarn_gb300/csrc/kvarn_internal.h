@@ -14,6 +14,11 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
                           cudaStream_t stream);
 
+cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_k, void* k_codes,
+                             void* k_params, float* k_scale, const void* v_x, int64_t n_v, void* v_codes,
+                             void* v_params, float* v_scale, int iters, int rotate, int normalize,
+                             cudaStream_t stream);
+
 cudaError_t launch_dequant(int bits, int kind, const void* codes, const void* params,
                            const float* tile_scale, int64_t n_tiles, int original_basis,
                            int rotate, float* out, cudaStream_t stream);

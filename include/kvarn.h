@@ -116,6 +116,17 @@ kvarn_status kvarn_encode_blocks(const kvarn_config* cfg, kvarn_kind kind, const
                                  int64_t n_tiles, void* codes, void* params, float* tile_scale,
                                  kvarn_stream_t stream);
 
+/* Encode n_tiles K blocks and n_tiles V blocks (the same token range of both caches) in one
+ * launch: the results are those of kvarn_encode_blocks(K) and kvarn_encode_blocks(V) on the same
+ * arguments, bit for bit [paperlayer, "3 Methods" and "D Experimental details": keys and values
+ * are normalised and quantised alike, with their own group axes]: one call for the usual case
+ * of appending a block to both caches.  Arguments, layouts and errors as for
+ * kvarn_encode_blocks, per kind (k_* with cfg->k_bits, v_* with cfg->v_bits). */
+kvarn_status kvarn_encode_kv_blocks(const kvarn_config* cfg, const void* k_bf16, const void* v_bf16,
+                                    int64_t n_tiles, void* k_codes, void* k_params, float* k_scale,
+                                    void* v_codes, void* v_params, float* v_scale,
+                                    kvarn_stream_t stream);
+
 /* Dequantise n_tiles packed tiles to float32 [n_tiles][128][128] (token-major).
  * original_basis = 0 returns Yhat (rotated basis); 1 returns Yhat * H, the estimate of the
  * input tile [paperlayer, "I KVarN Dequantization Overhead": both scales are applied in one

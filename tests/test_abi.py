@@ -83,6 +83,19 @@ def test_encode_validation_needs_no_gpu(lib):
     assert enc(ctypes.byref(cfg), 0, None, 0, None, None, None, None) == 0  # empty: no-op
 
 
+def test_fused_encode_validation_needs_no_gpu(lib):
+    cfg = _cfg()
+    enc = lib.kvarn_encode_kv_blocks
+    assert enc(None, FAKE, FAKE, 1, *[FAKE] * 6, None) == 1
+    assert enc(ctypes.byref(cfg), FAKE, FAKE, -1, *[FAKE] * 6, None) == 1
+    assert enc(ctypes.byref(cfg), FAKE, None, 1, *[FAKE] * 6, None) == 1
+    assert b"v_bf16" in lib.kvarn_last_error()
+    assert enc(ctypes.byref(cfg), FAKE, FAKE, 1, FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(cfg), FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE + 8, FAKE, FAKE, None) == 1
+    assert enc(ctypes.byref(_cfg(v_bits=3)), FAKE, FAKE, 1, *[FAKE] * 6, None) == 1
+    assert enc(ctypes.byref(cfg), None, None, 0, *[None] * 6, None) == 0
+
+
 def test_dequant_validation_needs_no_gpu(lib):
     cfg = _cfg()
     dq = lib.kvarn_dequant

@@ -95,6 +95,29 @@ def test_persistent_grid_many_tiles_and_empty(kv):
 
 
 @pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+@pytest.mark.parametrize("n", [512, 77, 1])
+def test_fused_kv_encode_equals_separate_calls(kv, preset, n):
+    # one launch over K and V tiles gives the two single-kind results bit for bit; the first
+    # fused tiles are also checked against the oracle directly
+    k, v = kv.synthetic.outlier_kv(11, n, 128, device="cuda")
+    k, v = k.reshape(n, 128, 128), v.reshape(n, 128, 128)
+    cfg = kv.kvarn_config_from_preset(preset)
+    ref_k = _encode_gpu(kv, cfg, kv.KVARN_KIND_K, k)
+    ref_v = _encode_gpu(kv, cfg, kv.KVARN_KIND_V, v)
+    out_k = [torch.full_like(t, 7) for t in ref_k]
+    out_v = [torch.full_like(t, 7) for t in ref_v]
+    kv.kvarn_encode_kv_blocks(cfg, k, v, *out_k, *out_v)
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_error() == 0
+    for got, want in zip(out_k + out_v, list(ref_k) + list(ref_v)):
+        assert torch.equal(got, want)
+    m = min(n, 4)
+    for name, x, res, bits in (("K", k, out_k, cfg.k_bits), ("V", v, out_v, cfg.v_bits)):
+        compare_encode(x[:m].float().cpu().double().numpy(), name, bits, res[0][:m].cpu().numpy(),
+                       res[1][:m].cpu().numpy(), res[2][:m].cpu().numpy())
+
+
+@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
 def test_dequant_matches_oracle_on_identical_packed_input(kv, preset):
     cfg = kv.kvarn_config_from_preset(preset)
     k, v = kv.synthetic.outlier_kv(8, 40, 128, device="cuda")
