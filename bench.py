@@ -14,6 +14,7 @@ bounded sample of the same workload, scaled to the same unit.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -79,7 +80,7 @@ def ncu_traffic(kernel):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -92,7 +93,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -107,25 +108,35 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
+    def summary(self, t0, t1):
+        """Samples taken between host times t0 and t1 (the timed region, widened by one polling
+        interval); if the region is shorter than the interval, the sample nearest to it."""
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+        inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+        if not inside and rows:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": inside[-1][2] if inside else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -177,16 +188,20 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    # each oracle step is a bounded sample (>= one tile pair and one decode unit, ~1.5 s); at most
+    # 20 timed and 1 warm-up step are run so the arm ends within a minute or two whatever K is
+    n_warm, n_timed = min(args.warmup, 1), max(1, min(args.steps, 20))
     times = []
     sample = ""
-    for i in range(args.warmup + args.steps):
-        us, sample = oracle_step_estimate(budget_s=max(2.0, 60.0 / (args.warmup + args.steps)))
-        if i >= args.warmup:
+    for i in range(n_warm + n_timed):
+        us, sample = oracle_step_estimate(budget_s=max(1.5, 60.0 / (n_warm + n_timed)))
+        if i >= n_warm:
             times.append(us)
     v = statistics.mean(times)
+    sample += f"; {n_timed} timed oracle steps (of {args.steps} requested) after {n_warm} warm-up"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": args.gpus, "steps": n_timed, "warmup": n_warm,
         "ms_per_step": round(v / 1000, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": "cache > L2; CPU run"},
@@ -277,6 +292,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     do_enc = args.only in ("all", "encode")
     do_dec = args.only in ("all", "decode")
+    clocks = ClockSampler(local).__enter__()  # polling from before the warm-up on
     for _ in range(args.warmup):
         l2_flush()
         if do_enc:
@@ -291,20 +307,22 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
-        for s in range(args.steps):
-            l2_flush()
-            a, b, c = marks[s]
-            a.record()
-            if do_enc:
-                enc()
-            b.record()
-            if do_dec:
-                dec()
-            c.record()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+    t_region0 = time.time()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        l2_flush()
+        a, b, c = marks[s]
+        a.record()
+        if do_enc:
+            enc()
+        b.record()
+        if do_dec:
+            dec()
+        c.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    t_region1 = time.time()
+    clocks.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
     enc_ms = [a.elapsed_time(b) for a, b, _ in marks]
@@ -377,7 +395,7 @@ def run_gpu(args):
                     "h2d_bytes_per_step": 2 * ek.numel() * 2 + q.numel() * 2,
                     "d2h_bytes_per_step": out.numel() * 4},
             "gpu_launches": (2 * do_enc + 3 * do_dec) * args.steps,
-            "clocks": clocks.summary(),
+            "clocks": clocks.summary(t_region0, t_region1),
             "wall_s_timed_region": round(t_wall, 4),
         }
         if not args.no_cpu_baseline:
@@ -392,7 +410,7 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
