@@ -627,12 +627,6 @@ decode_split_kernel(DecodeArgs a) {
                 }
                 tc::commit(&mmab[wk]);
             }
-            // while the MMAs run: refill the stage the previous tile used (every thread of the
-            // worker is past it: they all reached the barrier above)
-            if (pos > 0 && issued < piece.len) {
-                issue_copies(issued);
-                ++issued;
-            }
             ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;
             tc::fence_after();
@@ -727,6 +721,12 @@ decode_split_kernel(DecodeArgs a) {
                                    kIdesc, u);
                 }
                 tc::commit(&mmab[wk]);
+            }
+            // while the PV MMAs run: refill the stage the previous tile used (every thread of the
+            // worker is past it: they all reached this tile's barriers)
+            if (pos > 0 && issued < piece.len) {
+                issue_copies(issued);
+                ++issued;
             }
             ok = mbar_wait(&mmab[wk], mma_phase, &g_decode_error) && ok;
             mma_phase ^= 1;

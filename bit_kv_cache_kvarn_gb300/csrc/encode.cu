@@ -16,6 +16,7 @@
 // one packed FFMA2 per element: token sums reduce over 16 lanes by shuffles, channel sums over
 // the two half-warps by a shuffle and over the 8 warps through shared memory.
 #include <climits>
+#include <type_traits>
 
 #include "kvarn_common.cuh"
 #include "kvarn_internal.h"
@@ -35,7 +36,7 @@ struct EncodeSmem {
     float ys[kTile * kYStride];            // FWHT staging (72 KB)
     float2 red[kWarps][4][32];             // cross-warp partial sums (8 KB)
     float2 aa[kTile];                      // (1/c, 1/c^2) per channel
-    float cfac[kTile];                     // channel factor c
+    float cinv[kTile];                     // inverse channel factor 1 / c
     float logf_[kTile];                    // log of the other-axis factor
     float grp_min[kTile];
     float grp_scale[kTile];
@@ -129,7 +130,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         for (int it = 0; it < 4; ++it) {
             const int idx = tid + kThreads * it;
             const int t = idx >> 3, c = idx & 7;
-            float v[16];
+            float2 f[8];  // channels 16 c + 2 m, 16 c + 2 m + 1 in f[m]
             {
                 // the two 16-byte halves are read in a lane-dependent order (bank-conflict free)
                 const int sw = (c >> 2) & 1;
@@ -140,21 +141,17 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                 const __nv_bfloat162* p1 = reinterpret_cast<const __nv_bfloat162*>(&r1);
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    const float2 f0 = __bfloat1622float2(p0[m]);
-                    const float2 f1 = __bfloat1622float2(p1[m]);
-                    v[2 * m] = f0.x;
-                    v[2 * m + 1] = f0.y;
-                    v[8 + 2 * m] = f1.x;
-                    v[8 + 2 * m + 1] = f1.y;
+                    f[m] = __bfloat1622float2(p0[m]);
+                    f[4 + m] = __bfloat1622float2(p1[m]);
                 }
             }
-            if (rotate) fwht_regs<16>(v);
+            if (rotate) fwht_pairs<8>(f);
             float* dst = sm.ys + t * kYStride + 16 * c;
             {
                 // 16-byte chunks stored in a lane-dependent rotation (bank-conflict free)
                 const int rot = (c >> 1) & 3;
-                float4 a0 = make_float4(v[0], v[1], v[2], v[3]), a1 = make_float4(v[4], v[5], v[6], v[7]);
-                float4 a2 = make_float4(v[8], v[9], v[10], v[11]), a3 = make_float4(v[12], v[13], v[14], v[15]);
+                float4 a0 = make_float4(f[0].x, f[0].y, f[1].x, f[1].y), a1 = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+                float4 a2 = make_float4(f[4].x, f[4].y, f[5].x, f[5].y), a3 = make_float4(f[6].x, f[6].y, f[7].x, f[7].y);
                 rotl4(a0, a1, a2, a3, rot);
                 *reinterpret_cast<float4*>(dst + 4 * ((0 + rot) & 3)) = a0;
                 *reinterpret_cast<float4*>(dst + 4 * ((1 + rot) & 3)) = a1;
@@ -178,27 +175,33 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int t = tg + 16 * k;
-            float v[8];
+            float2 f[4];  // channels h + 16 (2 q), h + 16 (2 q + 1) in f[q]
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = sm.ys[t * kYStride + h + 16 * i];
+            for (int q = 0; q < 4; ++q)
+                f[q] = make_float2(sm.ys[t * kYStride + h + 32 * q], sm.ys[t * kYStride + h + 32 * q + 16]);
             if (rotate) {
-                fwht_regs<8>(v);
+                fwht_pairs<4>(f);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] *= kInvSqrt128;
+                for (int q = 0; q < 4; ++q) f[q] = fmul2(f[q], make_float2(kInvSqrt128, kInvSqrt128));
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) yy[k][i] = make_float2(v[i], v[i] * v[i]);
+            for (int q = 0; q < 4; ++q) {
+                const float2 sq = fmul2(f[q], f[q]);
+                yy[k][2 * q] = make_float2(f[q].x, sq.x);
+                yy[k][2 * q + 1] = make_float2(f[q].y, sq.y);
+            }
         }
 
         // ---- dual-axis variance normalisation ----
         // token step:   r_t = std_j(Y_tj / c_j)   (lane owns token kown of its 8 for the update)
         // channel step: c_j = std_t(Y_tj / r_t)
+        // The factors are kept as their inverses b = 1/r, a = 1/c (one rsqrt each).
         const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
-        float r_own = 1.f;
+        float b_own = 1.f;
         float2 aa[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) aa[i] = make_float2(1.f, 1.f);
-        if (tid < kTile) sm.cfac[tid] = 1.f;
+        if (tid < kTile) sm.cinv[tid] = 1.f;
         const int n_it = normalize ? iters : 0;
         for (int itn = 0; itn < n_it; ++itn) {
             // token step
@@ -215,8 +218,8 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                 const bool up = (h & 8) != 0;
                 float2 send = up ? acc[q] : acc[q + 4];
                 float2 keep = up ? acc[q + 4] : acc[q];
-                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 8);
-                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 8);
+                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 8),
+                                                       __shfl_xor_sync(0xffffffffu, send.y, 8)));
                 acc[q] = keep;
             }
 #pragma unroll
@@ -224,24 +227,23 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                 const bool up = (h & 4) != 0;
                 float2 send = up ? acc[q] : acc[q + 2];
                 float2 keep = up ? acc[q + 2] : acc[q];
-                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 4);
-                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 4);
+                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
+                                                       __shfl_xor_sync(0xffffffffu, send.y, 4)));
                 acc[q] = keep;
             }
             {
                 const bool up = (h & 2) != 0;
                 float2 send = up ? acc[0] : acc[1];
                 float2 keep = up ? acc[1] : acc[0];
-                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 2);
-                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 2);
-                keep.x += __shfl_xor_sync(0xffffffffu, keep.x, 1);
-                keep.y += __shfl_xor_sync(0xffffffffu, keep.y, 1);
+                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 2),
+                                                       __shfl_xor_sync(0xffffffffu, send.y, 2)));
+                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, keep.x, 1),
+                                                       __shfl_xor_sync(0xffffffffu, keep.y, 1)));
                 const float mean = keep.x * (1.f / kTile);
                 const float ms = keep.y * (1.f / kTile);
                 const float var = ms - mean * mean;
-                if (var > kDegenerateRel * ms) r_own = sqrtf(var);
+                if (var > kDegenerateRel * ms) b_own = rsqrtf(var);
             }
-            const float b_own = 1.f / r_own;
             float2 bb[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -260,8 +262,8 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             for (int q = 0; q < 4; ++q) {
                 float2 send = tsub ? acc[q] : acc[q + 4];
                 float2 keep = tsub ? acc[q + 4] : acc[q];
-                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 16);
-                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 16);
+                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 16),
+                                                       __shfl_xor_sync(0xffffffffu, send.y, 16)));
                 sm.red[warp][q][lane] = keep;  // channel h + 16 (q + 4 tsub)
             }
             __syncthreads();
@@ -271,17 +273,14 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                 float2 s = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) {
-                    float2 p = sm.red[w][q][src_lane];
-                    s.x += p.x;
-                    s.y += p.y;
+                    s = fadd2(s, sm.red[w][q][src_lane]);
                 }
                 const float mean = s.x * (1.f / kTile);
                 const float ms = s.y * (1.f / kTile);
                 const float var = ms - mean * mean;
-                float c = sm.cfac[j];
-                if (var > kDegenerateRel * ms) c = sqrtf(var);
-                sm.cfac[j] = c;
-                const float a = 1.f / c;
+                float a = sm.cinv[j];
+                if (var > kDegenerateRel * ms) a = rsqrtf(var);
+                sm.cinv[j] = a;
                 sm.aa[j] = make_float2(a, a * a);
             }
             __syncthreads();
@@ -292,9 +291,9 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
         // K: other axis = token (factor r); V: other axis = channel (factor c).
         if (KIND == KVARN_KIND_K) {
-            if ((h & 1) == 0) sm.logf_[tg + 16 * kown] = logf(r_own);
+            if ((h & 1) == 0) sm.logf_[tg + 16 * kown] = -logf(b_own);
         } else {
-            if (tid < kTile) sm.logf_[tid] = logf(sm.cfac[tid]);
+            if (tid < kTile) sm.logf_[tid] = -logf(sm.cinv[tid]);
         }
         __syncthreads();
         const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[tid] : 0.f, tid) * (1.f / kTile);
@@ -424,25 +423,56 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         uint32_t packed[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) packed[q] = 0;
+        {
+            // group constants: K groups are this thread's 8 channels, V groups its 8 tokens
+            float nz[8], is1[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int t = tg + 16 * k;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * i) : t;
-                const float d = fmaf(yy[k][i].x, inv_g, -sm.grp_z[grp]);
-                float u = d * sm.grp_inv_s1[grp];
-                // Near a half-way point the reciprocal product can break an exact tie the wrong
-                // way; redo it with a correctly rounded division so ties go to even.
-                if (fabsf(u - floorf(u) - 0.5f) < 1e-4f && sm.grp_inv_s1[grp] > 0.f)
-                    u = __fdiv_rn(d, sm.grp_s1[grp]);
-                int c = __float2int_rn(u);
-                c = min(max(c, 0), kLevels);
-                if (KIND == KVARN_KIND_K)
-                    packed[k] |= (uint32_t)c << (BITS * i);
-                else
-                    packed[i] |= (uint32_t)c << (BITS * k);
+            for (int m = 0; m < 8; ++m) {
+                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * m) : (tg + 16 * m);
+                nz[m] = -sm.grp_z[grp];
+                is1[m] = sm.grp_inv_s1[grp];
             }
+            // Adding 1.5 * 2^23 rounds a value in [0, 2^22) to an integer (half to even) held in the
+            // low mantissa bits.  Exact half-way points occur in practice only without the rotation
+            // (bf16 inputs on a coarse grid); there a product with the rounded reciprocal can land
+            // on the wrong side, so near a half-way point the code is redone with a correctly
+            // rounded division.  With the rotation the check is left out.
+            constexpr float kRound = 12582912.f;
+            auto quantise = [&](auto tie_check) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const int g0 = (KIND == KVARN_KIND_K) ? i : k, g1 = (KIND == KVARN_KIND_K) ? i + 1 : k;
+                        const float2 d = ffma2(make_float2(yy[k][i].x, yy[k][i + 1].x), make_float2(inv_g, inv_g),
+                                               make_float2(nz[g0], nz[g1]));
+                        const float2 u = fmul2(d, make_float2(is1[g0], is1[g1]));
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int ii = i + e, ge = e ? g1 : g0;
+                            const float ue = e ? u.y : u.x;
+                            float v = fminf(fmaxf(ue, 0.f), (float)kLevels);
+                            float r = v + kRound;
+                            if (decltype(tie_check)::value) {
+                                if (fabsf(v - (r - kRound)) > 0.4999f && is1[ge] > 0.f) {
+                                    const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * k);
+                                    v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[grp]), 0.f), (float)kLevels);
+                                    r = v + kRound;
+                                }
+                            }
+                            const uint32_t c = __float_as_uint(r) & (uint32_t)kLevels;
+                            if (KIND == KVARN_KIND_K)
+                                packed[k] |= c << (BITS * ii);
+                            else
+                                packed[ii] |= c << (BITS * k);
+                        }
+                    }
+                }
+            };
+            if (rotate)
+                quantise(std::integral_constant<bool, false>());
+            else
+                quantise(std::integral_constant<bool, true>());
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {

@@ -147,6 +147,26 @@ __device__ __forceinline__ void fwht_regs(float (&v)[N]) {
     }
 }
 
+// Walsh-Hadamard butterflies over 2*N2 values held as N2 float2 pairs (element 2p in .x, 2p+1 in
+// .y), unnormalised: the stage inside a pair is scalar, the wider stages pair whole float2s, so
+// each of them is one FADD2 and one FFMA2 per two butterflies.
+template <int N2>
+__device__ __forceinline__ void fwht_pairs(float2 (&f)[N2]) {
+#pragma unroll
+    for (int p = 0; p < N2; ++p) f[p] = make_float2(f[p].x + f[p].y, f[p].x - f[p].y);
+#pragma unroll
+    for (int s = 1; s < N2; s <<= 1) {
+#pragma unroll
+        for (int p = 0; p < N2; ++p) {
+            if ((p & s) == 0) {
+                const float2 a = f[p], b = f[p + s];
+                f[p] = fadd2(a, b);
+                f[p + s] = ffma2(b, make_float2(-1.f, -1.f), a);
+            }
+        }
+    }
+}
+
 // 128-point transform of a vector held 4 values per lane (lane l holds elements 4l..4l+3):
 // two stages in registers, five across lanes.  Unnormalised.
 __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
