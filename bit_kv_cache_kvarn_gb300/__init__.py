@@ -21,6 +21,7 @@ KVARN_KIND_K = 0
 KVARN_KIND_V = 1
 KVARN_FLAG_NO_ROTATE = 1
 KVARN_FLAG_NO_NORMALIZE = 2
+KVARN_FLAG_FULL_TAIL = 4
 PARAM_BYTES = 512
 TILE = 128
 

@@ -56,6 +56,10 @@ constexpr uint32_t kBKStride = 256, kBNStride = 128;  // core-matrix strides of 
 constexpr float kLazy = 4.f;
 constexpr float kWScale = 8.f;
 constexpr float kTwo24 = 16777216.f;
+// The lo piece of a B value is stored times 2^11 (it is at most half an fp16 ulp of the hi piece,
+// so it stays below |x| and never overflows): unscaled it would be an fp16 subnormal for most
+// values and carry only a few bits; its column's sum is multiplied back by 2^-11 on readout.
+constexpr float kLoScale = 2048.f;
 
 // A worker's piece of the tile stream.  The stream lists, sequence by sequence and unit by unit
 // (unit = kv head x head block), the full tiles of each unit; a piece is a contiguous run of it.
@@ -81,6 +85,7 @@ struct DecodeArgs {
     const __nv_bfloat16* v_tail;
     float qscale;  // softmax scale * log2(e): scores are kept in the log2 domain
     int rotate;
+    int full_tail;  // the tail holds the last 1..128 tokens (else L mod 128)
     int splits;     // partial slots per (sequence, query head) = splits + 1
     int B;
     int units;      // units per sequence: kv heads x head blocks
@@ -92,9 +97,15 @@ struct DecodeArgs {
 };
 
 
-__device__ __forceinline__ int clamp_len(int len, int max_tiles) {
-    const int cap = max_tiles * kTile + (kTile - 1);
+__device__ __forceinline__ int clamp_len(int len, int max_tiles, int full_tail) {
+    const int cap = max_tiles * kTile + (full_tail ? kTile : kTile - 1);
     return len < 0 ? 0 : (len > cap ? cap : len);
+}
+
+// Full tiles read from the pools for a (clamped) length: all complete blocks, or all but the
+// most recent one when the tail keeps a full window.
+__device__ __forceinline__ int n_full_tiles(int len, int full_tail) {
+    return full_tail ? (len > 0 ? (len - 1) >> 7 : 0) : len >> 7;
 }
 
 // Shared-memory ring stage: K codes | V codes | K params | V params, one bulk copy each.
@@ -191,7 +202,8 @@ __device__ __forceinline__ void load_row(const uint8_t* base, int r, uint32_t (&
     }
 }
 
-// hi/lo fp16 pieces of GH values, packed as B rows 2h (hi) and 2h+1 (lo); rows >= 2*GH stay zero.
+// hi/lo fp16 pieces of GH values (lo scaled by kLoScale), packed as B rows 2h (hi) and 2h+1 (lo);
+// rows >= 2*GH stay zero.
 template <int GH>
 __device__ __forceinline__ void store_b(uint8_t* b, int kk, const float (&x)[GH]) {
     uint32_t w[8];
@@ -200,7 +212,7 @@ __device__ __forceinline__ void store_b(uint8_t* b, int kk, const float (&x)[GH]
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
         const __half hi = __float2half_rn(x[h]);
-        const __half lo = __float2half_rn(x[h] - __half2float(hi));
+        const __half lo = __float2half_rn((x[h] - __half2float(hi)) * kLoScale);
         const __half2 v = __halves2half2(hi, lo);
         w[h] = *reinterpret_cast<const uint32_t*>(&v);
     }
@@ -364,7 +376,7 @@ __device__ __forceinline__ bool named_sync_and(int id, int n, bool flag) {
 }
 
 __device__ __forceinline__ int full_tiles(const DecodeArgs& a, int b) {
-    return clamp_len(a.seq_lens[b], a.max_tiles) >> 7;
+    return n_full_tiles(clamp_len(a.seq_lens[b], a.max_tiles, a.full_tail), a.full_tail);
 }
 
 // Partial slot of (sequence b, query head hq, slot k): m, l, pad, pad, o[128].
@@ -645,7 +657,7 @@ decode_split_kernel(DecodeArgs a) {
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 const float zk = zks[h];
-                const float dot = dsum[2 * h] + dsum[2 * h + 1];
+                const float dot = fmaf(dsum[2 * h + 1], 1.f / kLoScale, dsum[2 * h]);
                 float ei;
                 if constexpr (kQReg) ei = ereg[h];
                 else ei = einv[h];
@@ -737,7 +749,7 @@ decode_split_kernel(DecodeArgs a) {
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 const float zv = zvs[h];
-                const float acc = dsum[2 * h] + dsum[2 * h + 1];
+                const float acc = fmaf(dsum[2 * h + 1], 1.f / kLoScale, dsum[2 * h]);
                 o[h] = fmaf(fmaf(acc, kTwo24 / kWScale, zv), chan, o[h]);
             }
         }
@@ -885,9 +897,9 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     const int lane = threadIdx.x;
     const int hq = blockIdx.x, b = blockIdx.y;
     const int kvh = hq / a.group;
-    const int len = clamp_len(a.seq_lens[b], a.max_tiles);
-    const int tail = len & 127;
-    const int nt = len >> 7;
+    const int len = clamp_len(a.seq_lens[b], a.max_tiles, a.full_tail);
+    const int nt = n_full_tiles(len, a.full_tail);
+    const int tail = len - nt * kTile;  // 0..127, or 1..128 with the full window
     const float* base = slot_ptr(a, b, hq, 0);
     // the slots this (sequence, head) has: one per 16-tile block and the unit-entry slot
     const int n_slots = nt > 0 ? (nt + kTilesPerSplit - 1) / kTilesPerSplit + 1 : 0;
@@ -1010,7 +1022,7 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
                           const void* v_codes, const void* v_params, const float* v_scale,
                           const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
                           const void* k_tail, const void* v_tail, float softmax_scale, int rotate,
-                          void* workspace, const DecodePlan& plan, float* out,
+                          int full_tail, void* workspace, const DecodePlan& plan, float* out,
                           cudaStream_t stream) {
     DecodeArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
@@ -1030,6 +1042,7 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.v_tail = static_cast<const __nv_bfloat16*>(v_tail);
     a.qscale = softmax_scale * kLog2e;
     a.rotate = rotate;
+    a.full_tail = full_tail;
     a.splits = plan.splits;
     a.B = B;
     const int gh = group;  // up to 8 heads x (hi, lo) fill the 16 MMA columns

@@ -45,7 +45,7 @@ kvarn_status check_cfg(const kvarn_config* cfg) {
         return fail(KVARN_ERR_INVALID_ARG, "v_bits = %d; supported: 2, 4", cfg->v_bits);
     if (cfg->sinkhorn_iters < 0 || cfg->sinkhorn_iters > 64)
         return fail(KVARN_ERR_INVALID_ARG, "sinkhorn_iters = %d; allowed 0..64", cfg->sinkhorn_iters);
-    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATE | KVARN_FLAG_NO_NORMALIZE))
+    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATE | KVARN_FLAG_NO_NORMALIZE | KVARN_FLAG_FULL_TAIL))
         return fail(KVARN_ERR_INVALID_ARG, "unknown flag bits 0x%x", cfg->flags);
     return KVARN_OK;
 }
@@ -197,7 +197,8 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
         KV_TRY(check_ptr(block_table, 4, "block_table"));
     }
     if (seq_lens_host) {
-        const long long cap = (long long)max_tiles * KVARN_TILE_TOKENS + (KVARN_TILE_TOKENS - 1);
+        const long long cap = (long long)max_tiles * KVARN_TILE_TOKENS +
+                              ((cfg->flags & KVARN_FLAG_FULL_TAIL) ? KVARN_TILE_TOKENS : KVARN_TILE_TOKENS - 1);
         for (int b = 0; b < B; ++b)
             if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
                 return fail(KVARN_ERR_INVALID_ARG, "seq_lens[%d] = %d outside 0..%lld", b, seq_lens_host[b], cap);
@@ -210,7 +211,8 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
     cudaError_t e = kvarn::launch_decode(cfg->k_bits, cfg->v_bits, Hq / Hkv, q_bf16, B, Hq, Hkv, k_codes,
                                          k_params, k_scale, v_codes, v_params, v_scale, block_table,
                                          max_tiles, seq_lens, k_tail_bf16, v_tail_bf16, softmax_scale,
-                                         !(cfg->flags & KVARN_FLAG_NO_ROTATE), workspace, plan, out,
+                                         !(cfg->flags & KVARN_FLAG_NO_ROTATE),
+                                         (cfg->flags & KVARN_FLAG_FULL_TAIL) != 0, workspace, plan, out,
                                          (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     return ok();

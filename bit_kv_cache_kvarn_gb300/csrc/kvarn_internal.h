@@ -38,7 +38,7 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
                           const void* v_codes, const void* v_params, const float* v_scale,
                           const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
                           const void* k_tail, const void* v_tail, float softmax_scale, int rotate,
-                          void* workspace, const DecodePlan& plan, float* out,
+                          int full_tail, void* workspace, const DecodePlan& plan, float* out,
                           cudaStream_t stream);
 
 }  // namespace kvarn

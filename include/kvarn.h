@@ -83,6 +83,12 @@ typedef enum { KVARN_KIND_K = 0, KVARN_KIND_V = 1 } kvarn_kind;
  * grouping [paperlayer, "5 Related Work"], with the scale stored as FP8 times the tile factor. */
 #define KVARN_FLAG_NO_ROTATE 1u
 #define KVARN_FLAG_NO_NORMALIZE 2u
+/* Decode only: a full FP16 recent window [paperlayer, "D Experimental details": the most recent
+ * tokens stay in FP16, R = 128].  Without the flag the tail holds the L mod 128 tokens after the
+ * last full block (0..127); with it the tail holds the last ((L - 1) mod 128) + 1 tokens (1..128,
+ * none when L = 0), so a block is read from the packed pool only once a newer token exists --
+ * the block pseudo-decode's convention, where a block's tokens see each other unquantised. */
+#define KVARN_FLAG_FULL_TAIL 4u
 
 typedef struct {
     int32_t k_bits;         /* 2 or 4 */
@@ -154,9 +160,11 @@ size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int H
  *                 holding tokens [128 i, 128 i + 128) of that sequence.
  *   seq_lens    : [B] int32 device array, tokens of context per sequence (0 allowed).
  *   seq_lens_host: optional [B] host copy; when given, every length is checked against
- *                 128*max_tiles + 127 before launch (device lengths are clamped in any case).
- *   k_tail_bf16, v_tail_bf16 : [B][Hkv][128][128] bfloat16, original basis; tokens
- *                 [128*floor(L/128), L) of sequence b are rows 0 .. L mod 128 - 1.
+ *                 128*max_tiles + 127 (+ 128 with KVARN_FLAG_FULL_TAIL) before launch (device
+ *                 lengths are clamped to the same bound in any case).
+ *   k_tail_bf16, v_tail_bf16 : [B][Hkv][128][128] bfloat16, original basis; with n = the number
+ *                 of full tiles read from the pools (floor(L/128), or floor((L-1)/128) with
+ *                 KVARN_FLAG_FULL_TAIL), tokens [128 n, L) of sequence b are rows 0 .. L-128n-1.
  *   softmax_scale: multiplies q.k before the softmax.
  *   workspace   : at least kvarn_decode_workspace_size(...) bytes of device memory.
  *   out         : [B][Hq][128] float32 attention output (original basis); a sequence of

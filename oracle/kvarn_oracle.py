@@ -394,11 +394,15 @@ def attention_single_query(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: f
 
 
 def gather_cache(k_codes, k_params, k_scale, v_codes, v_params, v_scale, tile_ids, length,
-                 k_tail, v_tail, k_bits, v_bits, rotate=True):
+                 k_tail, v_tail, k_bits, v_bits, rotate=True, full_tail=False):
     """Rebuild one (sequence, kv head)'s keys and values in the original basis, fp64:
-    dequantised full tiles (in block-table order) followed by the unquantised tail rows."""
-    n_full = length // TILE
-    tail = length % TILE
+    dequantised full tiles (in block-table order) followed by the unquantised tail rows.
+
+    The tail holds the tokens after the last full tile (L mod 128 of them), or with full_tail a
+    whole FP16 recent window of the last ((L - 1) mod 128) + 1 tokens ([paperlayer] "D
+    Experimental details": the most recent tokens stay in FP16, R = 128)."""
+    n_full = ((length - 1) // TILE if length > 0 else 0) if full_tail else length // TILE
+    tail = length - n_full * TILE
     ks, vs = [], []
     for i in range(n_full):
         t = int(tile_ids[i])
@@ -413,7 +417,8 @@ def gather_cache(k_codes, k_params, k_scale, v_codes, v_params, v_scale, tile_id
 
 def decode_attention(q, hq: int, hkv: int, k_codes, k_params, k_scale, v_codes, v_params,
                      v_scale, block_table, seq_lens, k_tail, v_tail, softmax_scale: float,
-                     k_bits: int, v_bits: int, rotate: bool = True, pairs=None):
+                     k_bits: int, v_bits: int, rotate: bool = True, pairs=None,
+                     full_tail: bool = False):
     """Decode attention over the packed cache, plain definition in the original basis.
 
     For query head h of sequence b, kv head = h // (hq // hkv) (grouped-query attention); keys
@@ -436,7 +441,7 @@ def decode_attention(q, hq: int, hkv: int, k_codes, k_params, k_scale, v_codes, 
                 continue
             kk, vv = gather_cache(k_codes, k_params, k_scale, v_codes, v_params, v_scale,
                                   block_table[b, kv], int(seq_lens[b]), k_tail[b, kv],
-                                  v_tail[b, kv], k_bits, v_bits, rotate)
+                                  v_tail[b, kv], k_bits, v_bits, rotate, full_tail)
             for h in heads:
                 if want is None or (b, h) in want:
                     out[b, h] = attention_single_query(q[b, h], kk, vv, softmax_scale)

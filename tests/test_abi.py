@@ -127,6 +127,11 @@ def test_decode_validation_needs_no_gpu(lib):
     assert _decode(lib, cfg, tail=None) == 1
     assert _decode(lib, cfg, lens_host=[5, 4 * 128 + 128]) == 1  # over 128*max_tiles + 127
     assert _decode(lib, cfg, lens_host=[-1, 3]) == 1
+    # the full FP16 window allows one more token per sequence, and only that
+    full = _cfg(flags=4)
+    assert _decode(lib, full, lens_host=[5, 4 * 128 + 129]) == 1
+    assert b"0..640" in lib.kvarn_last_error()
+    assert _decode(lib, _cfg(flags=8), lens_host=[5, 6]) == 1
     assert _decode(lib, cfg, ws_bytes=16) == 4
     assert b"workspace" in lib.kvarn_last_error()
     assert _decode(lib, cfg, B=0) == 0

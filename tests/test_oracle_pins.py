@@ -295,7 +295,8 @@ def test_attention_matches_sdpa():
         assert np.abs(o.attention_single_query(q, k, v, 0.2) - ref).max() <= 1e-12
 
 
-def test_decode_attention_gqa_and_tail_against_sdpa_on_dequantised_cache():
+@pytest.mark.parametrize("full_tail", [False, True])
+def test_decode_attention_gqa_and_tail_against_sdpa_on_dequantised_cache(full_tail):
     rng = np.random.default_rng(16)
     bsz, hq, hkv, max_tiles = 2, 4, 2, 3
     n_tiles = bsz * hkv * max_tiles
@@ -309,13 +310,15 @@ def test_decode_attention_gqa_and_tail_against_sdpa_on_dequantised_cache():
     v_tail = rng.standard_normal((bsz, hkv, 128, 128))
     q = rng.standard_normal((bsz, hq, 128))
     out = o.decode_attention(q, hq, hkv, kc, kp, ks, vc, vp, vs, table, lens, k_tail, v_tail,
-                             0.1, 4, 2)
+                             0.1, 4, 2, full_tail=full_tail)
     kd = o.dequant_blocks(kc, kp, ks, "K", 4, original_basis=True)
     vd = o.dequant_blocks(vc, vp, vs, "V", 2, original_basis=True)
     for b in range(bsz):
         for h in range(hq):
             kv = h // 2
-            nfull, tail = lens[b] // 128, lens[b] % 128
+            # full window: the last ((L - 1) mod 128) + 1 tokens come from the tail
+            nfull = (lens[b] - 1) // 128 if full_tail else lens[b] // 128
+            tail = lens[b] - 128 * nfull
             kk = np.concatenate([kd[table[b, kv, i]] for i in range(nfull)] + [k_tail[b, kv, :tail]])
             vv = np.concatenate([vd[table[b, kv, i]] for i in range(nfull)] + [v_tail[b, kv, :tail]])
             ref = torch.nn.functional.scaled_dot_product_attention(
@@ -330,11 +333,11 @@ def test_decode_attention_tail_only_is_unquantised_attention():
     k_tail = rng.standard_normal((1, 1, 128, 128))
     v_tail = rng.standard_normal((1, 1, 128, 128))
     empty = np.zeros((0, 4096), np.uint8)
-    for L in (0, 1, 127):
+    for L, full_tail in ((0, False), (1, False), (127, False), (0, True), (1, True), (128, True)):
         out = o.decode_attention(q, 2, 1, empty, np.zeros((0, 512), np.uint8), np.zeros(0),
                                  empty, np.zeros((0, 512), np.uint8), np.zeros(0),
                                  np.zeros((1, 1, 1), np.int64), np.array([L]), k_tail, v_tail,
-                                 0.3, 2, 2)
+                                 0.3, 2, 2, full_tail=full_tail)
         for h in range(2):
             if L == 0:
                 assert not out[0, h].any()
