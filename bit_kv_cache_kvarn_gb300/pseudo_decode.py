@@ -158,9 +158,11 @@ def run(kv, cfg, weights, x, hq: int, hkv: int, quantised: bool = True, capture=
     return attn, seconds
 
 
-def mae_curves(attn_q, attn_ref):
-    """mae[j][l] = mean |attn_q - attn_ref| of block j, layer l (a nested list of floats)."""
-    return [[float((a - b).abs().mean()) for a, b in zip(rq, rr)] for rq, rr in zip(attn_q, attn_ref)]
+def mae_curves(attn_q, attn_ref, relative: bool = False):
+    """mae[j][l] = mean |attn_q - attn_ref| of block j, layer l (a nested list of floats); with
+    relative=True divided by mean |attn_ref| of the same block and layer."""
+    return [[float((a - b).abs().mean() / (b.abs().mean() if relative else 1.0)) for a, b in zip(rq, rr)]
+            for rq, rr in zip(attn_q, attn_ref)]
 
 
 def main():
@@ -189,7 +191,8 @@ def main():
                     ("rtn_k2v2 (no rotation, no normalisation)", kv.make_config(k_bits=2, v_bits=2, sinkhorn_iters=0,
                                                                                 flags=3))):
         a, t = run(kv, c, w, x, args.hq, args.hkv, quantised=True)
-        res[name] = {"seconds": round(t, 3), "mae": mae_curves(a, ref)}
+        res[name] = {"seconds": round(t, 3), "mae": mae_curves(a, ref),
+                     "relative_mae": mae_curves(a, ref, relative=True)}
     print(json.dumps(res))
 
 
