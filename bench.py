@@ -49,6 +49,15 @@ def enc_bytes(n_tiles_per_kind, k_bits=2, v_bits=2):
     return inp, out
 
 
+# Encode arithmetic per element (FP32 FLOPs, an FMA counting 2): rotation 7 butterfly stages + the
+# 1/sqrt(128) scale (8); Y^2 (1); 8 normalisation iterations x (token step + channel step) x the two
+# sums sum(Y a), sum(Y^2 a^2) as FMAs (64); W = Y / s2 (1); (W/g - Z) * (1/S1), clamp and round (6).
+ENC_FLOPS_PER_ELEMENT = 80
+# FP32 peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz.  (A measured
+# FFMA2 loop reached 76.5 TFLOP/s at ~1990 MHz on this GPU.)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def dec_bytes(k_bits=2, v_bits=2):
     tiles = DEC_B * DEC_HKV * (DEC_L // 128)
     cache = tiles * ((128 * 16 * k_bits + 512 + 4) + (128 * 16 * v_bits + 512 + 4))
@@ -366,6 +375,7 @@ def run_gpu(args):
         d_cache, d_q, d_out = dec_bytes()
         enc_gbs = (e_in + e_out) / (enc_ms_m * 1e-3) / 1e9
         enc_in_gbs = e_in / (enc_ms_m * 1e-3) / 1e9
+        enc_tflops = 2 * n_enc * 128 * 128 * ENC_FLOPS_PER_ELEMENT / (enc_ms_m * 1e-3) / 1e12
         dec_alg = d_cache + d_q + d_out
         dec_gbs = dec_alg / (dec_ms_m * 1e-3) / 1e9
         traffic = ncu_traffic("kvarn_decode_attention")
@@ -381,7 +391,13 @@ def run_gpu(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "encode": {"us": round(enc_ms_m * 1000, 2), "gbs_bf16_input": round(enc_in_gbs, 1),
                        "gbs_read_plus_write": round(enc_gbs, 1), "hbm_frac": round(enc_gbs / hbm, 4),
-                       "bytes_per_step": e_in + e_out, "launches_per_step": 2},
+                       "bytes_per_step": e_in + e_out, "launches_per_step": 2,
+                       "alu_roofline": {
+                           "bound": "alu", "unit": "TFLOP/s",
+                           "achieved": round(enc_tflops, 2), "peak": round(FP32_PEAK_TFLOPS, 1),
+                           "frac": round(enc_tflops / FP32_PEAK_TFLOPS, 4),
+                           "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+                           "flops_per_element": ENC_FLOPS_PER_ELEMENT}},
             "decode": {"us": round(dec_ms_m * 1000, 2),
                        "tokens_per_s": round(DEC_B / (dec_ms_m * 1e-3), 1),
                        "kv_tokens_per_s": round(DEC_B * DEC_L / (dec_ms_m * 1e-3), 1),
