@@ -221,6 +221,22 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_diagnostics():
+    """E_M / E_D split and token-scale statistics of each preset on the encode workload."""
+    import torch
+
+    import bit_kv_cache_kvarn_gb300 as kv
+    from bit_kv_cache_kvarn_gb300 import diagnostics
+
+    kv.load()
+    n_enc = ENC_SEQ * ENC_HKV
+    k, v = kv.synthetic.outlier_kv(1, n_enc, 128, device="cuda")
+    res = diagnostics.run(kv, k.reshape(n_enc, 128, 128), v.reshape(n_enc, 128, 128))
+    torch.cuda.synchronize()
+    print(json.dumps({"impl": "diagnostics", "workload": WORKLOAD.split(" + ")[0], "tiles_per_kind": n_enc,
+                      "presets": res}), flush=True)
+
+
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
@@ -432,12 +448,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ctx", type=int, default=32768, help="decode context (profiling runs only)")
+    ap.add_argument("--diagnostics", action="store_true",
+                    help="print the codec's error diagnostics on the encode workload instead of timing")
     ap.add_argument("--only", default="all", choices=["all", "encode", "decode"],
                     help="time one part (profiling runs only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.diagnostics:
+        run_diagnostics()
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

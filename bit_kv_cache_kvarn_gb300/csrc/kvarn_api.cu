@@ -68,15 +68,28 @@ extern "C" {
 
 kvarn_status kvarn_config_from_preset(const char* name, kvarn_config* out) {
     if (!name || !out) return fail(KVARN_ERR_INVALID_ARG, "name or out is NULL");
-    if (strcmp(name, "kvarn_k4v2_g128") == 0) {
-        *out = kvarn_config{4, 2, 8, 0u};
-        return ok();
+    struct Preset {
+        const char* name;
+        kvarn_config cfg;
+    };
+    static const Preset kPresets[] = {
+        {"kvarn_k4v2_g128", {4, 2, 8, 0u}},
+        {"kvarn_k2v2_g128", {2, 2, 8, 0u}},
+        {"kvarn_k4v4_g128", {4, 4, 8, 0u}},
+        {"kvarn_k2v4_g128", {2, 4, 8, 0u}},
+        {"hadamard_k2v2_g128", {2, 2, 0, KVARN_FLAG_NO_NORMALIZE}},
+        {"kivi_k2v2_g128", {2, 2, 0, KVARN_FLAG_NO_ROTATE | KVARN_FLAG_NO_NORMALIZE}},
+    };
+    for (const Preset& p : kPresets) {
+        if (strcmp(name, p.name) == 0) {
+            *out = p.cfg;
+            return ok();
+        }
     }
-    if (strcmp(name, "kvarn_k2v2_g128") == 0) {
-        *out = kvarn_config{2, 2, 8, 0u};
-        return ok();
-    }
-    return fail(KVARN_ERR_INVALID_ARG, "unknown preset '%s' (known: kvarn_k4v2_g128, kvarn_k2v2_g128)", name);
+    return fail(KVARN_ERR_INVALID_ARG,
+                "unknown preset '%s' (known: kvarn_k4v2_g128, kvarn_k2v2_g128, kvarn_k4v4_g128, "
+                "kvarn_k2v4_g128, hadamard_k2v2_g128, kivi_k2v2_g128)",
+                name);
 }
 
 size_t kvarn_tile_code_bytes(int bits) {

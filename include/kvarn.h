@@ -97,9 +97,15 @@ typedef struct {
     uint32_t flags;         /* KVARN_FLAG_* */
 } kvarn_config;
 
-/* Fill *out from a preset name.  "kvarn_k4v2_g128": 4-bit K, 2-bit V, group 128, 8 iterations
- * (the shipped preset [dimensionstp, "3-1 Overview"]); "kvarn_k2v2_g128": all 2-bit (the
- * paper's experimental setting [paperlayer, "D Experimental details"]).
+/* Fill *out from a preset name.
+ *   "kvarn_k4v2_g128": 4-bit K, 2-bit V, group 128, 8 iterations (the shipped preset
+ *       [dimensionstp, "3-1 Overview"]);
+ *   "kvarn_k2v2_g128": all 2-bit (the paper's setting [paperlayer, "D Experimental details"]);
+ *   "kvarn_k4v4_g128", "kvarn_k2v4_g128": the other bit widths (other granularities trade
+ *       capacity against overhead [dimensionstp, "4-3 Engineering notes"]);
+ *   ablations through the same kernels [paperlayer, "4 Experiments", "B Full Token-Scale
+ *   Distribution Error"]: "hadamard_k2v2_g128" = rotation without normalisation,
+ *   "kivi_k2v2_g128" = neither, plain per-channel (K) / per-token (V) RTN.
  * Returns KVARN_ERR_INVALID_ARG for a NULL pointer or an unknown name. */
 kvarn_status kvarn_config_from_preset(const char* name, kvarn_config* out);
 

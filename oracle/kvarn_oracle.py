@@ -446,3 +446,42 @@ def decode_attention(q, hq: int, hkv: int, k_codes, k_params, k_scale, v_codes, 
                 if want is None or (b, h) in want:
                     out[b, h] = attention_single_query(q[b, h], kk, vv, softmax_scale)
     return out
+
+
+# ----------------------------------------------------------------------------------------------
+# Error diagnostics
+# ----------------------------------------------------------------------------------------------
+def error_decomposition(x: np.ndarray, x_hat: np.ndarray):
+    """Per-row split of the squared reconstruction error into a magnitude and a direction part,
+    ||x - x_hat||^2 = (||x|| - ||x_hat||)^2 + 2 ||x|| ||x_hat|| (1 - cos theta)  -- an identity
+    ([pheeree] "핵심 세 가지" §2, E_M and E_D).  x, x_hat: [T, d]; returns (E_M, E_D), each [T]."""
+    x = np.asarray(x, dtype=np.float64)
+    x_hat = np.asarray(x_hat, dtype=np.float64)
+    n = np.linalg.norm(x, axis=1)
+    nh = np.linalg.norm(x_hat, axis=1)
+    e_m = (n - nh) ** 2
+    e_d = 2.0 * (n * nh - np.sum(x * x_hat, axis=1))  # 2 |x| |x_hat| (1 - cos theta)
+    return e_m, e_d
+
+
+def magnitude_share_of_top_errors(e_m, e_d, fractions=(0.5, 0.1, 0.05, 0.01, 0.001)):
+    """For the rows with the largest total error (top fraction f of rows, at least one): the share
+    of their summed error that is magnitude error, sum E_M / sum (E_M + E_D) ([pheeree] "핵심 세
+    가지" §2: the share grows toward the largest errors)."""
+    e_m = np.asarray(e_m, dtype=np.float64)
+    tot = e_m + np.asarray(e_d, dtype=np.float64)
+    order = np.argsort(-tot, kind="stable")
+    out = {}
+    for f in fractions:
+        top = order[:max(1, int(round(f * tot.size)))]
+        s = tot[top].sum()
+        out[f] = float(e_m[top].sum() / s) if s > 0 else 0.0
+    return out
+
+
+def token_scale_ratio(x: np.ndarray, x_hat: np.ndarray) -> np.ndarray:
+    """||x_hat_t|| / ||x_t|| per row t: how well the token's scale survives quantisation
+    ([paperlayer] "B Full Token-Scale Distribution Error")."""
+    n = np.linalg.norm(np.asarray(x, dtype=np.float64), axis=1)
+    nh = np.linalg.norm(np.asarray(x_hat, dtype=np.float64), axis=1)
+    return np.where(n > 0, nh / np.where(n > 0, n, 1.0), 1.0)

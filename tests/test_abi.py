@@ -50,6 +50,10 @@ def test_presets_and_sizes(lib):
     assert (c.k_bits, c.v_bits, c.sinkhorn_iters, c.flags) == (4, 2, 8, 0)
     c = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
     assert (c.k_bits, c.v_bits, c.sinkhorn_iters) == (2, 2, 8)
+    for name, want in (("kvarn_k4v4_g128", (4, 4, 8, 0)), ("kvarn_k2v4_g128", (2, 4, 8, 0)),
+                       ("hadamard_k2v2_g128", (2, 2, 0, 2)), ("kivi_k2v2_g128", (2, 2, 0, 3))):
+        c = kv.kvarn_config_from_preset(name)
+        assert (c.k_bits, c.v_bits, c.sinkhorn_iters, c.flags) == want
     with pytest.raises(kv.KvarnError, match="unknown preset"):
         kv.kvarn_config_from_preset("kvarn_k3v3")
     assert kv.kvarn_tile_code_bytes(2) == 4096 and kv.kvarn_tile_code_bytes(4) == 8192

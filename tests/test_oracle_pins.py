@@ -345,3 +345,35 @@ def test_decode_attention_tail_only_is_unquantised_attention():
             s = 0.3 * k_tail[0, 0, :L] @ q[0, h]
             p = np.exp(s - s.max())
             assert np.abs(out[0, h] - (p / p.sum()) @ v_tail[0, 0, :L]).max() <= 1e-12
+
+
+# --- error diagnostics ------------------------------------------------------------------------
+def test_error_decomposition_identity_and_special_cases():
+    rng = np.random.default_rng(50)
+    x = rng.standard_normal((300, 128)) * np.exp(rng.standard_normal((300, 1)))
+    xh = x + 0.1 * rng.standard_normal((300, 128))
+    e_m, e_d = o.error_decomposition(x, xh)
+    total = np.sum((x - xh) ** 2, axis=1)
+    # E_D cancels terms of size |x|^2, so the identity holds to rounding of |x|^2
+    scale = np.sum(x * x, axis=1)
+    assert np.all(np.abs(e_m + e_d - total) <= 1e-13 * scale)
+    assert np.all(e_m >= 0) and np.all(e_d >= -1e-13 * scale)
+    # a pure rescaling is all magnitude error; a rotation of equal length is all direction error
+    e_m, e_d = o.error_decomposition(x, 1.5 * x)
+    assert np.all(np.abs(e_d) <= 1e-13 * scale)
+    assert np.allclose(e_m, 0.25 * np.sum(x * x, axis=1), rtol=1e-12)
+    rot = np.concatenate([x[:, 1:], x[:, :1]], axis=1)  # a permutation keeps the norm
+    e_m, e_d = o.error_decomposition(x, rot)
+    assert np.all(e_m <= 1e-24 * scale ** 2 + 1e-30)
+
+
+def test_magnitude_share_and_token_scale_ratio_by_hand():
+    e_m = np.array([0.0, 1.0, 3.0, 0.5])
+    e_d = np.array([1.0, 1.0, 1.0, 0.5])
+    s = o.magnitude_share_of_top_errors(e_m, e_d, fractions=(0.25, 0.5, 1.0))
+    assert s[0.25] == 3.0 / 4.0                     # the largest total error is row 2 (4.0)
+    assert s[0.5] == (3.0 + 1.0) / (4.0 + 2.0)      # rows 2 and 1
+    assert s[1.0] == 4.5 / 8.0
+    x = np.array([[3.0, 4.0], [0.0, 0.0], [1.0, 0.0]])
+    xh = np.array([[6.0, 8.0], [0.0, 1.0], [0.0, 0.5]])
+    assert np.allclose(o.token_scale_ratio(x, xh), [2.0, 1.0, 0.5])
