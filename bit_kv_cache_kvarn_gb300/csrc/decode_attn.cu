@@ -116,7 +116,8 @@ struct Stage {
     static constexpr uint32_t kKP = kV + VB * 2048;
     static constexpr uint32_t kVP = kKP + 512;
     static constexpr uint32_t kBytes = kVP + 512;
-    static constexpr int kCount = (KB + VB == 4) ? 3 : 2;
+    // ring depth: four stages at K2V2, three at mixed widths, two at K4V4 (2 CTAs per SM must fit)
+    static constexpr int kCount = (KB + VB == 4) ? 4 : (KB + VB == 6 ? 3 : 2);
 };
 
 // Byte offset of the 8 consecutive B elements (rows n0..n0+7) at K index kk.
@@ -415,7 +416,9 @@ decode_split_kernel(DecodeArgs a) {
 
     const int hblocks = a.hblocks;
     const int worker = blockIdx.x * kWorkers + wk;
-    const PlanEntry piece = a.plan[worker];
+    // programmatic dependent launch: the merge grid may be scheduled early (it waits for this
+    // grid before reading the workspace); this grid's prologue overlaps the plan kernel's tail
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     for (int i = tid; i < (int)(kWorkers * 2 * kBBytes / 16); i += kThreads) {
         const int wkr = i / (2 * kBBytes / 16), off = i % (2 * kBBytes / 16);
@@ -428,6 +431,8 @@ decode_split_kernel(DecodeArgs a) {
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan kernel's results are visible
+    const PlanEntry piece = a.plan[worker];
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const uint32_t a_col = tmem + 128 * wk, d_col = a_col + 64;  // D: 4 partials x 16 columns
@@ -828,6 +833,7 @@ decode_split_kernel(DecodeArgs a) {
 // of the tile stream -- equal shares of >= kMinPiece tiles, so the split kernel is balanced to a
 // tile whatever the length mix.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a, int n_workers) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ long long warp_tot[32];
     __shared__ long long carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -904,6 +910,7 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     // the slots this (sequence, head) has: one per 16-tile block and the unit-entry slot
     const int n_slots = nt > 0 ? (nt + kTilesPerSplit - 1) / kTilesPerSplit + 1 : 0;
     auto slot_of = [&](int i) { return i + 1 == n_slots ? a.splits : i; };
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel's partials are visible
 
     float mmax = -INFINITY;
     for (int i = lane; i < n_slots; i += 32) mmax = fmaxf(mmax, base[slot_of(i) * kWsStride]);
@@ -911,17 +918,31 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     float l = 0.f;
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     if (mmax != -INFINITY) {
-        for (int i = 0; i < n_slots; ++i) {
-            const int s = slot_of(i);
-            if (base[s * kWsStride] == -INFINITY) continue;  // an empty slot (o is not written)
-            const float f = exp2f(base[s * kWsStride] - mmax);
-            l = fmaf(base[s * kWsStride + 1], f, l);
-            const float4 v = *reinterpret_cast<const float4*>(base + s * kWsStride + 4 + 4 * lane);
-            o[0] = fmaf(v.x, f, o[0]);
-            o[1] = fmaf(v.y, f, o[1]);
-            o[2] = fmaf(v.z, f, o[2]);
-            o[3] = fmaf(v.w, f, o[3]);
+        // 32 slots at a time: each lane weighs one slot, then every lane adds the weighted o of
+        // each slot for its 4 channels (the loads of a chunk are independent of one another)
+        for (int c0 = 0; c0 < n_slots; c0 += 32) {
+            const int i = c0 + lane;
+            float f = 0.f;
+            if (i < n_slots) {
+                const float m = base[slot_of(i) * kWsStride];
+                if (m != -INFINITY) {  // an empty slot (its o is not written) weighs 0
+                    f = exp2f(m - mmax);
+                    l = fmaf(base[slot_of(i) * kWsStride + 1], f, l);
+                }
+            }
+            const int n_c = min(32, n_slots - c0);
+#pragma unroll 4
+            for (int j = 0; j < n_c; ++j) {
+                const float fj = __shfl_sync(0xffffffffu, f, j);
+                if (fj == 0.f) continue;
+                const float4 v = *reinterpret_cast<const float4*>(base + slot_of(c0 + j) * kWsStride + 4 + 4 * lane);
+                o[0] = fmaf(v.x, fj, o[0]);
+                o[1] = fmaf(v.y, fj, o[1]);
+                o[2] = fmaf(v.z, fj, o[2]);
+                o[3] = fmaf(v.w, fj, o[3]);
+            }
         }
+        l = warp_sum(l);
         if (a.rotate) {
             fwht128_warp(o, lane);
 #pragma unroll
@@ -966,6 +987,24 @@ size_t split_smem_bytes() {
     return bytes < 80 * 1024 ? 80 * 1024 : bytes;
 }
 
+// Launch with programmatic stream serialisation: the grid may start before the previous kernel in
+// the stream completes; it executes griddepcontrol.wait before reading that kernel's results.
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             const DecodeArgs& a) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, a);
+}
+
 int split_grid() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -981,8 +1020,7 @@ cudaError_t run_split(const DecodeArgs& a, int grid, cudaStream_t stream) {
     const size_t smem = split_smem_bytes<KB, VB, GH>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int KB, int VB>
@@ -1062,8 +1100,7 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, grid, stream);
     else e = run_split_g<4, 4>(a, gh, grid, stream);
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<<<dim3(Hq, B), 32, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(decode_merge_kernel, dim3(Hq, B), dim3(32), 0, stream, a);
 }
 
 }  // namespace kvarn
