@@ -171,10 +171,15 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         }
 
         // ---- rotation pass 2: H_8 over channel bits 4..6; thread keeps (Y, Y^2) ----
+        // Register slot k of a thread holds token tg + 16 (k ^ kown), kown = channel-lane bits 3..1
+        // as a 3-bit number: the partner lanes of the token reductions (h ^ 8, h ^ 4, h ^ 2) then
+        // hold each other's tokens in complementary slots, so every lane keeps and sends the same
+        // slots and no per-lane selection is needed; after the reduction lane h owns token kown.
+        const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
         float2 yy[8][8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const int t = tg + 16 * k;
+            const int t = tg + 16 * (k ^ kown);
             float2 f[4];  // channels h + 16 (2 q), h + 16 (2 q + 1) in f[q]
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -196,7 +201,6 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         // token step:   r_t = std_j(Y_tj / c_j)   (lane owns token kown of its 8 for the update)
         // channel step: c_j = std_t(Y_tj / r_t)
         // The factors are kept as their inverses b = 1/r, a = 1/c (one rsqrt each).
-        const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
         float b_own = 1.f;
         float2 aa[8];
 #pragma unroll
@@ -215,26 +219,23 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             // transposing reduction over the 16 channel lanes
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const bool up = (h & 8) != 0;
-                float2 send = up ? acc[q] : acc[q + 4];
-                float2 keep = up ? acc[q + 4] : acc[q];
+                const float2 send = acc[q + 4];
+                float2 keep = acc[q];
                 keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 8),
                                                        __shfl_xor_sync(0xffffffffu, send.y, 8)));
                 acc[q] = keep;
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const bool up = (h & 4) != 0;
-                float2 send = up ? acc[q] : acc[q + 2];
-                float2 keep = up ? acc[q + 2] : acc[q];
+                const float2 send = acc[q + 2];
+                float2 keep = acc[q];
                 keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
                                                        __shfl_xor_sync(0xffffffffu, send.y, 4)));
                 acc[q] = keep;
             }
             {
-                const bool up = (h & 2) != 0;
-                float2 send = up ? acc[0] : acc[1];
-                float2 keep = up ? acc[1] : acc[0];
+                const float2 send = acc[1];
+                float2 keep = acc[0];
                 keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 2),
                                                        __shfl_xor_sync(0xffffffffu, send.y, 2)));
                 keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, keep.x, 1),
@@ -247,7 +248,8 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             float2 bb[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int src = (lane & 16) | (((k >> 2) & 1) << 3) | (((k >> 1) & 1) << 2) | ((k & 1) << 1);
+                const int kt = k ^ kown;  // the lane owning slot k's token has kown == kt
+                const int src = (lane & 16) | (((kt >> 2) & 1) << 3) | (((kt >> 1) & 1) << 2) | ((kt & 1) << 1);
                 const float b = __shfl_sync(0xffffffffu, b_own, src);
                 bb[k] = make_float2(b, b * b);
             }
@@ -311,7 +313,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             float2 mm[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float inv = sm.oth_inv_s2[tg + 16 * k];
+                const float inv = sm.oth_inv_s2[tg + 16 * (k ^ kown)];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) yy[k][i].x *= inv;
             }
@@ -365,26 +367,23 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const bool up = (h & 8) != 0;
-                float2 send = up ? mm[q] : mm[q + 4];
-                float2 keep = up ? mm[q + 4] : mm[q];
+                const float2 send = mm[q + 4];
+                float2 keep = mm[q];
                 keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 8));
                 keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 8));
                 mm[q] = keep;
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const bool up = (h & 4) != 0;
-                float2 send = up ? mm[q] : mm[q + 2];
-                float2 keep = up ? mm[q + 2] : mm[q];
+                const float2 send = mm[q + 2];
+                float2 keep = mm[q];
                 keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 4));
                 keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 4));
                 mm[q] = keep;
             }
             {
-                const bool up = (h & 2) != 0;
-                float2 send = up ? mm[0] : mm[1];
-                float2 keep = up ? mm[1] : mm[0];
+                const float2 send = mm[1];
+                float2 keep = mm[0];
                 keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 2));
                 keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 2));
                 keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, keep.x, 1));
@@ -428,7 +427,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
             float nz[8], is1[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * m) : (tg + 16 * m);
+                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * m) : (tg + 16 * (m ^ kown));
                 nz[m] = -sm.grp_z[grp];
                 is1[m] = sm.grp_inv_s1[grp];
             }
@@ -455,7 +454,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                             float r = v + kRound;
                             if (decltype(tie_check)::value) {
                                 if (fabsf(v - (r - kRound)) > 0.4999f && is1[ge] > 0.f) {
-                                    const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * k);
+                                    const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * (k ^ kown));
                                     v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[grp]), 0.f), (float)kLevels);
                                     r = v + kRound;
                                 }
@@ -464,7 +463,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
                             if (KIND == KVARN_KIND_K)
                                 packed[k] |= c << (BITS * ii);
                             else
-                                packed[ii] |= c << (BITS * k);
+                                packed[ii] |= c << (BITS * (k ^ kown));
                         }
                     }
                 }
@@ -476,7 +475,7 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const int row = (KIND == KVARN_KIND_K) ? (tg + 16 * q) : (h + 16 * q);
+            const int row = (KIND == KVARN_KIND_K) ? (tg + 16 * (q ^ kown)) : (h + 16 * q);
             const int lane16 = (KIND == KVARN_KIND_K) ? h : tg;
             if (BITS == 2)
                 reinterpret_cast<uint16_t*>(sm.codes)[row * 16 + lane16] = (uint16_t)packed[q];
