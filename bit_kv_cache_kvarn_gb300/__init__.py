@@ -59,6 +59,9 @@ _SIGNATURES = {
     "kvarn_decode_attention": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
                                       ctypes.c_float, _vp, _sz, _vp, _vp]),
+    "kvarn_decode_attention_sink": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
+                                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
+                                           _i32, _vp, _vp, ctypes.c_float, _vp, _sz, _vp, _vp]),
     "kvarn_decode_attention_static_ws": (_i32, [ctypes.POINTER(kvarn_config), _vp, _i32, _i32, _i32,
                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                                                 _vp, _vp, ctypes.c_float, _vp, _vp]),
@@ -192,9 +195,11 @@ def kvarn_decode_workspace_size(cfg: kvarn_config, B: int, Hq: int, Hkv: int, ma
 
 def kvarn_decode_attention(cfg: kvarn_config, q, Hkv: int, k_codes, k_params, k_scale, v_codes,
                            v_params, v_scale, block_table, seq_lens, k_tail, v_tail,
-                           softmax_scale: float, workspace, out, seq_lens_host=None, stream=None):
+                           softmax_scale: float, workspace, out, seq_lens_host=None, stream=None,
+                           k_sink=None, v_sink=None, sink_len: int = 0):
     """q: [B, Hq, 128] bf16; block_table: [B, Hkv, max_tiles] int32; seq_lens: [B] int32 (device);
-    tails: [B, Hkv, 128, 128] bf16; out: [B, Hq, 128] float32."""
+    tails: [B, Hkv, 128, 128] bf16; out: [B, Hq, 128] float32.  With sink_len > 0 the first
+    sink_len tokens come from k_sink / v_sink ([B, Hkv, 128, 128] bf16; kvarn_decode_attention_sink)."""
     B, Hq = q.shape[0], q.shape[1]
     max_tiles = block_table.shape[-1]
     _need(q, torch.bfloat16, B * Hq * TILE, "q")
@@ -208,6 +213,15 @@ def kvarn_decode_attention(cfg: kvarn_config, q, Hkv: int, k_codes, k_params, k_
         arr = (ctypes.c_int32 * B)(*[int(v) for v in seq_lens_host])
         host = ctypes.cast(arr, ctypes.c_void_p)
     ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
+    if sink_len:
+        _need(k_sink, torch.bfloat16, B * Hkv * TILE * TILE, "k_sink")
+        _need(v_sink, torch.bfloat16, B * Hkv * TILE * TILE, "v_sink")
+        _check(load().kvarn_decode_attention_sink(
+            ctypes.byref(cfg), _ptr(q), B, Hq, Hkv, _ptr(k_codes), _ptr(k_params), _ptr(k_scale),
+            _ptr(v_codes), _ptr(v_params), _ptr(v_scale), _ptr(block_table), max_tiles, _ptr(seq_lens),
+            host, _ptr(k_sink), _ptr(v_sink), int(sink_len), _ptr(k_tail), _ptr(v_tail),
+            float(softmax_scale), _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+        return
     _check(load().kvarn_decode_attention(
         ctypes.byref(cfg), _ptr(q), B, Hq, Hkv, _ptr(k_codes), _ptr(k_params), _ptr(k_scale),
         _ptr(v_codes), _ptr(v_params), _ptr(v_scale), _ptr(block_table), max_tiles, _ptr(seq_lens),

@@ -81,6 +81,9 @@ struct DecodeArgs {
     const int32_t* block_table;
     int max_tiles;
     const int32_t* seq_lens;
+    const __nv_bfloat16* k_sink;  // [B][Hkv][128][128] bf16, the first sink_len tokens (or null)
+    const __nv_bfloat16* v_sink;
+    int sink_len;                 // 0..128 FP16 sink tokens before the packed body
     const __nv_bfloat16* k_tail;
     const __nv_bfloat16* v_tail;
     float qscale;  // softmax scale * log2(e): scores are kept in the log2 domain
@@ -376,8 +379,14 @@ __device__ __forceinline__ bool named_sync_and(int id, int n, bool flag) {
     return out != 0;
 }
 
+// Length of the body (packed tiles + tail) of sequence b: the tokens after the sink.
+__device__ __forceinline__ int body_len(const DecodeArgs& a, int b) {
+    const int len = a.seq_lens[b] - a.sink_len;
+    return clamp_len(len, a.max_tiles, a.full_tail);
+}
+
 __device__ __forceinline__ int full_tiles(const DecodeArgs& a, int b) {
-    return n_full_tiles(clamp_len(a.seq_lens[b], a.max_tiles, a.full_tail), a.full_tail);
+    return n_full_tiles(body_len(a, b), a.full_tail);
 }
 
 // Partial slot of (sequence b, query head hq, slot k): m, l, pad, pad, o[128].
@@ -903,9 +912,10 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     const int lane = threadIdx.x;
     const int hq = blockIdx.x, b = blockIdx.y;
     const int kvh = hq / a.group;
-    const int len = clamp_len(a.seq_lens[b], a.max_tiles, a.full_tail);
+    const int len = body_len(a, b);
     const int nt = n_full_tiles(len, a.full_tail);
     const int tail = len - nt * kTile;  // 0..127, or 1..128 with the full window
+    const int n_sink = max(0, min(a.sink_len, a.seq_lens[b]));
     const float* base = slot_ptr(a, b, hq, 0);
     // the slots this (sequence, head) has: one per 16-tile block and the unit-entry slot
     const int n_slots = nt > 0 ? (nt + kTilesPerSplit - 1) / kTilesPerSplit + 1 : 0;
@@ -949,15 +959,18 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
             for (int m = 0; m < 4; ++m) o[m] *= kInvSqrt128;
         }
     }
-    if (tail > 0) {
+    if (tail > 0 || n_sink > 0) {
+        // the unquantised tokens: the FP16 sink, then the tail, in the original basis
         const __nv_bfloat16* qp = a.q + ((size_t)b * a.Hq + hq) * kTile + 4 * lane;
         float qv[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) qv[m] = __bfloat162float(qp[m]) * a.qscale;
         const size_t tb = ((size_t)b * a.Hkv + kvh) * kTile * kTile;
-        for (int t = 0; t < tail; ++t) {
-            const __nv_bfloat16* kt = a.k_tail + tb + (size_t)t * kTile + 4 * lane;
-            const __nv_bfloat16* vt = a.v_tail + tb + (size_t)t * kTile + 4 * lane;
+        for (int t = 0; t < n_sink + tail; ++t) {
+            const bool in_sink = t < n_sink;
+            const size_t row = tb + (size_t)(in_sink ? t : t - n_sink) * kTile + 4 * lane;
+            const __nv_bfloat16* kt = (in_sink ? a.k_sink : a.k_tail) + row;
+            const __nv_bfloat16* vt = (in_sink ? a.v_sink : a.v_tail) + row;
             float d = 0.f;
 #pragma unroll
             for (int m = 0; m < 4; ++m) d = fmaf(qv[m], __bfloat162float(kt[m]), d);
@@ -1059,9 +1072,9 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
                           const void* k_codes, const void* k_params, const float* k_scale,
                           const void* v_codes, const void* v_params, const float* v_scale,
                           const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
-                          const void* k_tail, const void* v_tail, float softmax_scale, int rotate,
-                          int full_tail, void* workspace, const DecodePlan& plan, float* out,
-                          cudaStream_t stream) {
+                          const void* k_sink, const void* v_sink, int sink_len, const void* k_tail,
+                          const void* v_tail, float softmax_scale, int rotate, int full_tail,
+                          void* workspace, const DecodePlan& plan, float* out, cudaStream_t stream) {
     DecodeArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.Hq = Hq;
@@ -1076,6 +1089,9 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.block_table = block_table;
     a.max_tiles = max_tiles;
     a.seq_lens = seq_lens;
+    a.k_sink = static_cast<const __nv_bfloat16*>(k_sink);
+    a.v_sink = static_cast<const __nv_bfloat16*>(v_sink);
+    a.sink_len = sink_len;
     a.k_tail = static_cast<const __nv_bfloat16*>(k_tail);
     a.v_tail = static_cast<const __nv_bfloat16*>(v_tail);
     a.qscale = softmax_scale * kLog2e;

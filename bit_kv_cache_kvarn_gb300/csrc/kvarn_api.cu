@@ -183,23 +183,30 @@ size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int H
     return kvarn::plan_decode(B, Hq, Hkv, max_tiles).workspace_bytes;
 }
 
-kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
-                                    int Hkv, const void* k_codes, const void* k_params,
-                                    const float* k_scale, const void* v_codes,
-                                    const void* v_params, const float* v_scale,
-                                    const int32_t* block_table, int max_tiles,
-                                    const int32_t* seq_lens, const int32_t* seq_lens_host,
-                                    const void* k_tail_bf16, const void* v_tail_bf16,
-                                    float softmax_scale, void* workspace, size_t workspace_bytes,
-                                    float* out, kvarn_stream_t stream) {
+namespace {
+
+kvarn_status decode_impl(const kvarn_config* cfg, const void* q_bf16, int B, int Hq, int Hkv,
+                         const void* k_codes, const void* k_params, const float* k_scale,
+                         const void* v_codes, const void* v_params, const float* v_scale,
+                         const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
+                         const int32_t* seq_lens_host, const void* k_sink_bf16, const void* v_sink_bf16,
+                         int sink_len, const void* k_tail_bf16, const void* v_tail_bf16,
+                         float softmax_scale, void* workspace, size_t workspace_bytes, float* out,
+                         kvarn_stream_t stream) {
     KV_TRY(check_decode_shape(cfg, B, Hq, Hkv, max_tiles));
     if (!isfinite(softmax_scale)) return fail(KVARN_ERR_INVALID_ARG, "softmax_scale is not finite");
+    if (sink_len < 0 || sink_len > KVARN_TILE_TOKENS)
+        return fail(KVARN_ERR_INVALID_ARG, "sink_len = %d outside 0..128", sink_len);
     if (B == 0) return ok();
     KV_TRY(check_ptr(q_bf16, 16, "q_bf16"));
     KV_TRY(check_ptr(seq_lens, 4, "seq_lens"));
     KV_TRY(check_ptr(k_tail_bf16, 16, "k_tail_bf16"));
     KV_TRY(check_ptr(v_tail_bf16, 16, "v_tail_bf16"));
     KV_TRY(check_ptr(out, 16, "out"));
+    if (sink_len > 0) {
+        KV_TRY(check_ptr(k_sink_bf16, 16, "k_sink_bf16"));
+        KV_TRY(check_ptr(v_sink_bf16, 16, "v_sink_bf16"));
+    }
     if (max_tiles > 0) {
         KV_TRY(check_ptr(k_codes, 16, "k_codes"));
         KV_TRY(check_ptr(k_params, 16, "k_params"));
@@ -210,7 +217,7 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
         KV_TRY(check_ptr(block_table, 4, "block_table"));
     }
     if (seq_lens_host) {
-        const long long cap = (long long)max_tiles * KVARN_TILE_TOKENS +
+        const long long cap = (long long)sink_len + (long long)max_tiles * KVARN_TILE_TOKENS +
                               ((cfg->flags & KVARN_FLAG_FULL_TAIL) ? KVARN_TILE_TOKENS : KVARN_TILE_TOKENS - 1);
         for (int b = 0; b < B; ++b)
             if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap)
@@ -223,12 +230,42 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
                     plan.workspace_bytes);
     cudaError_t e = kvarn::launch_decode(cfg->k_bits, cfg->v_bits, Hq / Hkv, q_bf16, B, Hq, Hkv, k_codes,
                                          k_params, k_scale, v_codes, v_params, v_scale, block_table,
-                                         max_tiles, seq_lens, k_tail_bf16, v_tail_bf16, softmax_scale,
-                                         !(cfg->flags & KVARN_FLAG_NO_ROTATE),
+                                         max_tiles, seq_lens, k_sink_bf16, v_sink_bf16, sink_len, k_tail_bf16,
+                                         v_tail_bf16, softmax_scale, !(cfg->flags & KVARN_FLAG_NO_ROTATE),
                                          (cfg->flags & KVARN_FLAG_FULL_TAIL) != 0, workspace, plan, out,
                                          (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     return ok();
+}
+
+}  // namespace
+
+kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
+                                    int Hkv, const void* k_codes, const void* k_params,
+                                    const float* k_scale, const void* v_codes,
+                                    const void* v_params, const float* v_scale,
+                                    const int32_t* block_table, int max_tiles,
+                                    const int32_t* seq_lens, const int32_t* seq_lens_host,
+                                    const void* k_tail_bf16, const void* v_tail_bf16,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    float* out, kvarn_stream_t stream) {
+    return decode_impl(cfg, q_bf16, B, Hq, Hkv, k_codes, k_params, k_scale, v_codes, v_params, v_scale,
+                       block_table, max_tiles, seq_lens, seq_lens_host, nullptr, nullptr, 0, k_tail_bf16,
+                       v_tail_bf16, softmax_scale, workspace, workspace_bytes, out, stream);
+}
+
+kvarn_status kvarn_decode_attention_sink(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
+                                         int Hkv, const void* k_codes, const void* k_params,
+                                         const float* k_scale, const void* v_codes, const void* v_params,
+                                         const float* v_scale, const int32_t* block_table, int max_tiles,
+                                         const int32_t* seq_lens, const int32_t* seq_lens_host,
+                                         const void* k_sink_bf16, const void* v_sink_bf16, int sink_len,
+                                         const void* k_tail_bf16, const void* v_tail_bf16,
+                                         float softmax_scale, void* workspace, size_t workspace_bytes,
+                                         float* out, kvarn_stream_t stream) {
+    return decode_impl(cfg, q_bf16, B, Hq, Hkv, k_codes, k_params, k_scale, v_codes, v_params, v_scale,
+                       block_table, max_tiles, seq_lens, seq_lens_host, k_sink_bf16, v_sink_bf16, sink_len,
+                       k_tail_bf16, v_tail_bf16, softmax_scale, workspace, workspace_bytes, out, stream);
 }
 
 kvarn_status kvarn_device_error(uint32_t* code_out) {

@@ -37,8 +37,8 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
                           const void* k_codes, const void* k_params, const float* k_scale,
                           const void* v_codes, const void* v_params, const float* v_scale,
                           const int32_t* block_table, int max_tiles, const int32_t* seq_lens,
-                          const void* k_tail, const void* v_tail, float softmax_scale, int rotate,
-                          int full_tail, void* workspace, const DecodePlan& plan, float* out,
-                          cudaStream_t stream);
+                          const void* k_sink, const void* v_sink, int sink_len, const void* k_tail,
+                          const void* v_tail, float softmax_scale, int rotate, int full_tail,
+                          void* workspace, const DecodePlan& plan, float* out, cudaStream_t stream);
 
 }  // namespace kvarn

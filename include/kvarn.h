@@ -187,6 +187,29 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16,
                                     float softmax_scale, void* workspace, size_t workspace_bytes,
                                     float* out, kvarn_stream_t stream);
 
+/* Decode attention with an FP16 sink: the first min(sink_len, L) tokens of each sequence are kept
+ * unquantised [paperlayer, "D Experimental details": FP16 sink tokens, a grouped quantised body and
+ * FP16 trailing tokens; S = 128, or 32 for one benchmark].  Arguments as for
+ * kvarn_decode_attention, plus
+ *   k_sink_bf16, v_sink_bf16 : [B][Hkv][128][128] bfloat16, original basis; rows 0 .. S'-1 hold
+ *                 the sink tokens of sequence b, S' = min(sink_len, L) (may be NULL when
+ *                 sink_len = 0);
+ *   sink_len    : 0..128.
+ * seq_lens counts all tokens (sink, body and tail); the block table and the tail then describe the
+ * body of L - S' tokens exactly as kvarn_decode_attention describes a whole sequence (entry i of
+ * the block table holds body tokens [128 i, 128 i + 128), i.e. tokens S + 128 i ...), and the
+ * seq_lens_host bound grows by sink_len.  Attention does not depend on the order of the keys, so
+ * the sink is attended like the tail.  kvarn_decode_attention is this call with sink_len = 0. */
+kvarn_status kvarn_decode_attention_sink(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
+                                         int Hkv, const void* k_codes, const void* k_params,
+                                         const float* k_scale, const void* v_codes, const void* v_params,
+                                         const float* v_scale, const int32_t* block_table, int max_tiles,
+                                         const int32_t* seq_lens, const int32_t* seq_lens_host,
+                                         const void* k_sink_bf16, const void* v_sink_bf16, int sink_len,
+                                         const void* k_tail_bf16, const void* v_tail_bf16,
+                                         float softmax_scale, void* workspace, size_t workspace_bytes,
+                                         float* out, kvarn_stream_t stream);
+
 /* Decode attention without a caller workspace.  Same arguments and results as
  * kvarn_decode_attention, minus workspace/workspace_bytes: the split-K partials go to a fixed array
  * of KVARN_STATIC_WS_BYTES (8 MiB) that the library keeps in device memory on every GPU that loads

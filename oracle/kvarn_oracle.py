@@ -418,7 +418,7 @@ def gather_cache(k_codes, k_params, k_scale, v_codes, v_params, v_scale, tile_id
 def decode_attention(q, hq: int, hkv: int, k_codes, k_params, k_scale, v_codes, v_params,
                      v_scale, block_table, seq_lens, k_tail, v_tail, softmax_scale: float,
                      k_bits: int, v_bits: int, rotate: bool = True, pairs=None,
-                     full_tail: bool = False):
+                     full_tail: bool = False, k_sink=None, v_sink=None, sink_len: int = 0):
     """Decode attention over the packed cache, plain definition in the original basis.
 
     For query head h of sequence b, kv head = h // (hq // hkv) (grouped-query attention); keys
@@ -428,6 +428,9 @@ def decode_attention(q, hq: int, hkv: int, k_codes, k_params, k_scale, v_codes, 
     ([paperlayer] "A Hadamard Transform Arrangement").
     q: [B, hq, 128]; block_table: [B, hkv, max_tiles]; tails: [B, hkv, 128, 128].
     pairs: optional list of (b, h) to compute (others stay NaN), for sampled checks.
+    With sink_len > 0 the first min(sink_len, L) tokens are FP16 sink rows (k_sink, v_sink:
+    [B, hkv, 128, 128]) and the block table and tail describe the remaining body ([paperlayer] "D
+    Experimental details": FP16 sink tokens before the quantised body).
     """
     q = np.asarray(q, dtype=np.float64)
     bsz = q.shape[0]
@@ -439,9 +442,13 @@ def decode_attention(q, hq: int, hkv: int, k_codes, k_params, k_scale, v_codes, 
             heads = [kv * group + g for g in range(group)]
             if want is not None and not any((b, h) in want for h in heads):
                 continue
+            n_sink = min(sink_len, int(seq_lens[b]))
             kk, vv = gather_cache(k_codes, k_params, k_scale, v_codes, v_params, v_scale,
-                                  block_table[b, kv], int(seq_lens[b]), k_tail[b, kv],
+                                  block_table[b, kv], int(seq_lens[b]) - n_sink, k_tail[b, kv],
                                   v_tail[b, kv], k_bits, v_bits, rotate, full_tail)
+            if n_sink:
+                kk = np.concatenate([np.asarray(k_sink[b, kv], dtype=np.float64)[:n_sink], kk], axis=0)
+                vv = np.concatenate([np.asarray(v_sink[b, kv], dtype=np.float64)[:n_sink], vv], axis=0)
             for h in heads:
                 if want is None or (b, h) in want:
                     out[b, h] = attention_single_query(q[b, h], kk, vv, softmax_scale)

@@ -120,6 +120,27 @@ def _decode(lib, cfg, B=2, Hq=8, Hkv=2, max_tiles=4, lens_host=None, ws=FAKE, ws
                                       ctypes.c_float(scale), ws, ws_bytes, FAKE, None)
 
 
+def test_sink_decode_validation_needs_no_gpu(lib):
+    cfg = _cfg()
+
+    def call(sink_len, sink=FAKE, lens_host=None, B=2):
+        host = None
+        if lens_host is not None:
+            arr = (ctypes.c_int32 * len(lens_host))(*lens_host)
+            host = ctypes.cast(arr, ctypes.c_void_p)
+        return lib.kvarn_decode_attention_sink(ctypes.byref(cfg), FAKE, B, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                               FAKE, FAKE, 4, FAKE, host, sink, sink, sink_len, FAKE, FAKE,
+                                               ctypes.c_float(0.1), FAKE, 1 << 30, FAKE, None)
+
+    assert call(129) == 1
+    assert call(-1) == 1
+    assert call(32, sink=None) == 1
+    assert b"k_sink" in lib.kvarn_last_error()
+    assert call(32, lens_host=[5, 32 + 4 * 128 + 128]) == 1  # body over 128*max_tiles + 127
+    assert b"0..671" in lib.kvarn_last_error()
+    assert call(32, B=0) == 0
+
+
 def test_decode_validation_needs_no_gpu(lib):
     cfg = _cfg()
     assert _decode(lib, cfg, Hq=6, Hkv=4) == 1

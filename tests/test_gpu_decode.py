@@ -153,6 +153,37 @@ def test_plain_gaussian_cache_with_moderately_sharp_softmax(kv, k_bits, v_bits):
     print("gaussian worst rel-L2", check(gpu, oracle_out(cfg, q, hkv, c, 1 / math.sqrt(128))))
 
 
+@pytest.mark.parametrize("sink_len,flags", [(128, 0), (32, 0), (32, 4)])
+def test_fp16_sink(kv, sink_len, flags):
+    # the first sink_len tokens come from a bf16 sink buffer, the body from the packed pool and the
+    # tail; lengths shorter than the sink, equal to it, and with a body of full tiles and a tail
+    cfg = kv.make_config(4, 2, 8, flags)
+    lens = [0, 7, sink_len, sink_len + 1, sink_len + 128, sink_len + 3 * 128 + 45]
+    body = [max(0, L - sink_len) for L in lens]
+    c = build_cache(kv, cfg, len(lens), 2, body, seed=19)
+    g = torch.Generator(device="cpu").manual_seed(19)
+    k_sink = torch.randn(len(lens), 2, 128, 128, generator=g).to(torch.bfloat16).cuda()
+    v_sink = torch.randn(len(lens), 2, 128, 128, generator=g).to(torch.bfloat16).cuda()
+    q = kv.synthetic.queries(19, len(lens), 8, device="cuda")
+    ws = torch.empty(kv.kvarn_decode_workspace_size(cfg, len(lens), 8, 2, c["nt"]) // 4 + 4, device="cuda")
+    out = torch.full((len(lens), 8, 128), float("nan"), device="cuda")
+    kc, kp, ks = c["pools"]["k"]
+    vc, vp, vs = c["pools"]["v"]
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kv.kvarn_decode_attention(cfg, q, 2, kc, kp, ks, vc, vp, vs, c["table"], lens_t, c["k_tail"], c["v_tail"],
+                              0.08, ws, out, seq_lens_host=lens, k_sink=k_sink, v_sink=v_sink, sink_len=sink_len)
+    torch.cuda.synchronize()
+    kc, kp, ks = (t.cpu().numpy() for t in c["pools"]["k"])
+    vc, vp, vs = (t.cpu().numpy() for t in c["pools"]["v"])
+    ref = o.decode_attention(q.float().cpu().double().numpy(), 8, 2, kc, kp, ks, vc, vp, vs,
+                             c["table"].cpu().numpy(), lens, c["k_tail"].float().cpu().numpy(),
+                             c["v_tail"].float().cpu().numpy(), 0.08, 4, 2, full_tail=bool(flags & 4),
+                             k_sink=k_sink.float().cpu().numpy(), v_sink=v_sink.float().cpu().numpy(),
+                             sink_len=sink_len)
+    print("sink", sink_len, "worst rel-L2", check(out, ref))
+    assert torch.all(out[0] == 0)
+
+
 def test_no_rotate_flag(kv):
     cfg = kv.make_config(4, 2, 8, 1)
     lens = [7 * 128 + 3]

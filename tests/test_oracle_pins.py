@@ -377,3 +377,32 @@ def test_magnitude_share_and_token_scale_ratio_by_hand():
     x = np.array([[3.0, 4.0], [0.0, 0.0], [1.0, 0.0]])
     xh = np.array([[6.0, 8.0], [0.0, 1.0], [0.0, 0.5]])
     assert np.allclose(o.token_scale_ratio(x, xh), [2.0, 1.0, 0.5])
+
+
+def test_decode_attention_with_sink_against_sdpa():
+    # FP16 sink rows come first, then the dequantised body tiles, then the tail
+    rng = np.random.default_rng(18)
+    bsz, hq, hkv, max_tiles = 3, 2, 1, 2
+    n_tiles = bsz * hkv * max_tiles
+    kc, kp, ks, _ = o.encode_blocks(np.stack([_outlier_tile(300 + i) for i in range(n_tiles)]), "K", 2)
+    vc, vp, vs, _ = o.encode_blocks(np.stack([_outlier_tile(400 + i) for i in range(n_tiles)]), "V", 2)
+    table = rng.permutation(n_tiles).reshape(bsz, hkv, max_tiles)
+    lens = np.array([20, 32 + 128 + 5, 32 + 2 * 128 + 100])
+    k_sink, v_sink = rng.standard_normal((bsz, hkv, 128, 128)), rng.standard_normal((bsz, hkv, 128, 128))
+    k_tail, v_tail = rng.standard_normal((bsz, hkv, 128, 128)), rng.standard_normal((bsz, hkv, 128, 128))
+    q = rng.standard_normal((bsz, hq, 128))
+    out = o.decode_attention(q, hq, hkv, kc, kp, ks, vc, vp, vs, table, lens, k_tail, v_tail, 0.1, 2, 2,
+                             k_sink=k_sink, v_sink=v_sink, sink_len=32)
+    kd = o.dequant_blocks(kc, kp, ks, "K", 2, original_basis=True)
+    vd = o.dequant_blocks(vc, vp, vs, "V", 2, original_basis=True)
+    for b in range(bsz):
+        ns = min(32, lens[b])
+        body = lens[b] - ns
+        nfull, tail = body // 128, body % 128
+        kk = np.concatenate([k_sink[b, 0, :ns]] + [kd[table[b, 0, i]] for i in range(nfull)] + [k_tail[b, 0, :tail]])
+        vv = np.concatenate([v_sink[b, 0, :ns]] + [vd[table[b, 0, i]] for i in range(nfull)] + [v_tail[b, 0, :tail]])
+        for h in range(hq):
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q[b, h])[None, None, None], torch.from_numpy(kk)[None, None],
+                torch.from_numpy(vv)[None, None], scale=0.1)[0, 0, 0].numpy()
+            assert np.abs(out[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
