@@ -66,6 +66,9 @@ _SIGNATURES = {
                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                                                 _vp, _vp, ctypes.c_float, _vp, _vp]),
     "kvarn_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
+    "kvarn_append_workspace_size": (_sz, [_i32, _i32]),
+    "kvarn_append_tokens": (_i32, [ctypes.POINTER(kvarn_config), _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "kvarn_status_string": (ctypes.c_char_p, [_i32]),
     "kvarn_last_error": (ctypes.c_char_p, []),
 }
@@ -172,6 +175,31 @@ def kvarn_encode_kv_blocks(cfg: kvarn_config, k, v, k_codes, k_params, k_scale, 
     _check(load().kvarn_encode_kv_blocks(ctypes.byref(cfg), _ptr(k), _ptr(v), n_tiles, _ptr(k_codes),
                                          _ptr(k_params), _ptr(k_scale), _ptr(v_codes), _ptr(v_params),
                                          _ptr(v_scale), _stream(stream)))
+
+
+def kvarn_append_workspace_size(B: int, Hkv: int) -> int:
+    return int(load().kvarn_append_workspace_size(B, Hkv))
+
+
+def kvarn_append_tokens(cfg: kvarn_config, k_new, v_new, seq_lens, k_tail, v_tail, k_codes, k_params, k_scale,
+                        v_codes, v_params, v_scale, block_table, workspace, n_accept=None, stream=None):
+    """Commit offered tokens k_new, v_new [B, Hkv, n_new, 128] bf16 (the first n_accept[b] of
+    them, or all) to the tails / pools; seq_lens, tails and pools are updated in place."""
+    B, Hkv, n_new = k_new.shape[0], k_new.shape[1], k_new.shape[2]
+    max_tiles = block_table.shape[-1]
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, B * Hkv * n_new * TILE, name)
+    for t, name in ((k_tail, "k_tail"), (v_tail, "v_tail")):
+        _need(t, torch.bfloat16, B * Hkv * TILE * TILE, name)
+    _need(seq_lens, torch.int32, B, "seq_lens")
+    _need(block_table, torch.int32, B * Hkv * max_tiles, "block_table")
+    if n_accept is not None:
+        _need(n_accept, torch.int32, B, "n_accept")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().kvarn_append_tokens(ctypes.byref(cfg), B, Hkv, _ptr(k_new), _ptr(v_new), n_new, _ptr(n_accept),
+                                      _ptr(seq_lens), _ptr(k_tail), _ptr(v_tail), _ptr(k_codes), _ptr(k_params),
+                                      _ptr(k_scale), _ptr(v_codes), _ptr(v_params), _ptr(v_scale),
+                                      _ptr(block_table), max_tiles, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def kvarn_dequant(cfg: kvarn_config, kind: int, codes, params, tile_scale, out, original_basis=1,

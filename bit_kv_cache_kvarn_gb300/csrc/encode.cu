@@ -82,7 +82,8 @@ template <int BITS, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ codes_out,
               uint8_t* __restrict__ params_out, float* __restrict__ scale_out, int iters,
-              int rotate, int normalize) {
+              int rotate, int normalize, const int32_t* __restrict__ n_dev,
+              const int32_t* __restrict__ dest) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
     constexpr int kLevels = (1 << BITS) - 1;
@@ -94,6 +95,8 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
     const int h = lane & 15;                 // channel lane: channels h + 16 i
     const int tsub = lane >> 4;
     const int tg = 2 * warp + tsub;          // token group: tokens tg + 16 k
+    // optional device-side tile count (at most n_tiles) and output slots (dest[i] for input tile i)
+    if (n_dev != nullptr) n_tiles = min(n_tiles, (int64_t)max(*n_dev, 0));
 
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
@@ -487,14 +490,15 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
         // ---- write out: codes (16-byte stores), params, tile factor ----
         if (ok_data) {
             constexpr int kCodeBytes = kTile * 16 * BITS;
-            uint4* dst = reinterpret_cast<uint4*>(codes_out + tile * kCodeBytes);
+            const int64_t otile = dest != nullptr ? (int64_t)dest[tile] : tile;
+            uint4* dst = reinterpret_cast<uint4*>(codes_out + otile * kCodeBytes);
             const uint4* src = reinterpret_cast<const uint4*>(sm.codes);
 #pragma unroll
             for (int v = tid; v < kCodeBytes / 16; v += kThreads) dst[v] = src[v];
             if (tid < KVARN_PARAM_BYTES / 16)
-                reinterpret_cast<uint4*>(params_out + tile * KVARN_PARAM_BYTES)[tid] =
+                reinterpret_cast<uint4*>(params_out + otile * KVARN_PARAM_BYTES)[tid] =
                     reinterpret_cast<const uint4*>(sm.params)[tid];
-            if (tid == 0) scale_out[tile] = g;
+            if (tid == 0) scale_out[otile] = g;
         }
         __syncthreads();
     }
@@ -515,7 +519,7 @@ cudaError_t read_and_clear_device_error(unsigned int* out) {
 
 cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const int32_t* n_dev, const int32_t* dest) {
     int dev = 0, sms = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -529,7 +533,7 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
         kern<<<grid, kThreads, smem, stream>>>(static_cast<const __nv_bfloat16*>(x), n_tiles,
                                                static_cast<uint8_t*>(codes),
                                                static_cast<uint8_t*>(params), tile_scale, iters,
-                                               rotate, normalize);
+                                               rotate, normalize, n_dev, dest);
         return cudaGetLastError();
     };
     if (bits == 2 && kind == KVARN_KIND_K) return run(encode_kernel<2, KVARN_KIND_K>);

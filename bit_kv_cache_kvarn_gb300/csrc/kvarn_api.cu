@@ -278,7 +278,74 @@ kvarn_status kvarn_device_error(uint32_t* code_out) {
     unsigned int w = 0;
     e = kvarn::read_and_clear_decode_error(&w);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
-    *code_out = v | (w << 1);
+    unsigned int x = 0;
+    e = kvarn::read_and_clear_append_error(&x);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    *code_out = v | (w << 1) | (x << 2);
+    return ok();
+}
+
+size_t kvarn_append_workspace_size(int B, int Hkv) {
+    if (B < 0 || B > 65535 || Hkv < 1 || Hkv > 1024) return 0;
+    return kvarn::append_workspace_bytes(B, Hkv);
+}
+
+kvarn_status kvarn_append_tokens(const kvarn_config* cfg, int B, int Hkv, const void* k_new_bf16,
+                                 const void* v_new_bf16, int n_new, const int32_t* n_accept,
+                                 int32_t* seq_lens, void* k_tail_bf16, void* v_tail_bf16, void* k_codes,
+                                 void* k_params, float* k_scale, void* v_codes, void* v_params,
+                                 float* v_scale, const int32_t* block_table, int max_tiles, void* workspace,
+                                 size_t workspace_bytes, kvarn_stream_t stream) {
+    KV_TRY(check_cfg(cfg));
+    if (B < 0 || B > 65535) return fail(KVARN_ERR_INVALID_ARG, "B = %d outside 0..65535", B);
+    if (Hkv < 1 || Hkv > 1024) return fail(KVARN_ERR_INVALID_ARG, "Hkv = %d outside 1..1024", Hkv);
+    if (n_new < 1 || n_new > KVARN_TILE_TOKENS) return fail(KVARN_ERR_INVALID_ARG, "n_new = %d outside 1..128", n_new);
+    if (max_tiles < 0 || max_tiles > (1 << 24))
+        return fail(KVARN_ERR_INVALID_ARG, "max_tiles = %d outside 0..2^24", max_tiles);
+    if (B == 0) return ok();
+    KV_TRY(check_ptr(k_new_bf16, 16, "k_new_bf16"));
+    KV_TRY(check_ptr(v_new_bf16, 16, "v_new_bf16"));
+    if (n_accept) KV_TRY(check_ptr(n_accept, 4, "n_accept"));
+    KV_TRY(check_ptr(seq_lens, 4, "seq_lens"));
+    KV_TRY(check_ptr(k_tail_bf16, 16, "k_tail_bf16"));
+    KV_TRY(check_ptr(v_tail_bf16, 16, "v_tail_bf16"));
+    if (max_tiles > 0) {
+        KV_TRY(check_ptr(k_codes, 16, "k_codes"));
+        KV_TRY(check_ptr(k_params, 16, "k_params"));
+        KV_TRY(check_ptr(k_scale, 4, "k_scale"));
+        KV_TRY(check_ptr(v_codes, 16, "v_codes"));
+        KV_TRY(check_ptr(v_params, 16, "v_params"));
+        KV_TRY(check_ptr(v_scale, 4, "v_scale"));
+        KV_TRY(check_ptr(block_table, 4, "block_table"));
+    }
+    KV_TRY(check_ptr(workspace, 256, "workspace"));
+    const size_t need = kvarn::append_workspace_bytes(B, Hkv);
+    if (workspace_bytes < need)
+        return fail(KVARN_ERR_WORKSPACE, "workspace_bytes = %zu < required %zu", workspace_bytes, need);
+    kvarn::AppendArgs a;
+    a.Hkv = Hkv;
+    a.n_new = n_new;
+    a.max_tiles = max_tiles;
+    a.full_tail = (cfg->flags & KVARN_FLAG_FULL_TAIL) != 0;
+    a.k_new = static_cast<const __nv_bfloat16*>(k_new_bf16);
+    a.v_new = static_cast<const __nv_bfloat16*>(v_new_bf16);
+    a.n_accept = n_accept;
+    a.seq_lens = seq_lens;
+    a.k_tail = static_cast<__nv_bfloat16*>(k_tail_bf16);
+    a.v_tail = static_cast<__nv_bfloat16*>(v_tail_bf16);
+    a.block_table = block_table;
+    const size_t tiles = (size_t)B * Hkv;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    a.k_stage = reinterpret_cast<__nv_bfloat16*>(w);
+    a.v_stage = reinterpret_cast<__nv_bfloat16*>(w + tiles * KVARN_TILE_TOKENS * KVARN_TILE_TOKENS * 2);
+    a.dest = reinterpret_cast<int32_t*>(w + 2 * tiles * KVARN_TILE_TOKENS * KVARN_TILE_TOKENS * 2);
+    a.count = reinterpret_cast<int32_t*>(w + 2 * tiles * KVARN_TILE_TOKENS * KVARN_TILE_TOKENS * 2 +
+                                         ((tiles * sizeof(int32_t) + 255) & ~(size_t)255));
+    cudaError_t e = kvarn::launch_append(a, B, cfg->k_bits, cfg->v_bits, cfg->sinkhorn_iters,
+                                         !(cfg->flags & KVARN_FLAG_NO_ROTATE),
+                                         !(cfg->flags & KVARN_FLAG_NO_NORMALIZE), k_codes, k_params, k_scale,
+                                         v_codes, v_params, v_scale, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return ok();
 }
 

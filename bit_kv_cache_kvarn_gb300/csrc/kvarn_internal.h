@@ -1,6 +1,7 @@
 // Launchers behind the libkvarn C-ABI (host side, not exported).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,9 +11,12 @@ namespace kvarn {
 size_t encode_smem_bytes();
 cudaError_t read_and_clear_device_error(unsigned int* out);
 cudaError_t read_and_clear_decode_error(unsigned int* out);
+// n_dev (optional): device-side tile count, at most n_tiles; dest (optional): output slot of input
+// tile i.
 cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const int32_t* n_dev = nullptr,
+                          const int32_t* dest = nullptr);
 
 cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_k, void* k_codes,
                              void* k_params, float* k_scale, const void* v_x, int64_t n_v, void* v_codes,
@@ -40,5 +44,26 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
                           const void* k_sink, const void* v_sink, int sink_len, const void* k_tail,
                           const void* v_tail, float softmax_scale, int rotate, int full_tail,
                           void* workspace, const DecodePlan& plan, float* out, cudaStream_t stream);
+
+// Appending tokens: arguments of the append kernel (all device pointers).
+struct AppendArgs {
+    int Hkv, n_new, max_tiles, full_tail;
+    const __nv_bfloat16* k_new;  // [B][Hkv][n_new][128]
+    const __nv_bfloat16* v_new;
+    const int32_t* n_accept;     // [B] or null (all offered tokens)
+    int32_t* seq_lens;           // [B], updated
+    __nv_bfloat16* k_tail;       // [B][Hkv][128][128], updated
+    __nv_bfloat16* v_tail;
+    const int32_t* block_table;  // [B][Hkv][max_tiles]
+    __nv_bfloat16* k_stage;      // workspace: [B * Hkv][128][128] staged blocks
+    __nv_bfloat16* v_stage;
+    int32_t* dest;               // workspace: [B * Hkv] pool slot of each staged tile
+    int32_t* count;              // workspace: number of staged tiles
+};
+size_t append_workspace_bytes(int B, int Hkv);
+cudaError_t launch_append(const AppendArgs& a, int B, int k_bits, int v_bits, int iters, int rotate,
+                          int normalize, void* k_codes, void* k_params, float* k_scale, void* v_codes,
+                          void* v_params, float* v_scale, cudaStream_t stream);
+cudaError_t read_and_clear_append_error(unsigned int* out);
 
 }  // namespace kvarn

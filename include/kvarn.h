@@ -233,9 +233,39 @@ kvarn_status kvarn_decode_attention_static_ws(
     const int32_t* seq_lens_host, const void* k_tail_bf16, const void* v_tail_bf16,
     float softmax_scale, float* out, kvarn_stream_t stream);
 
-/* Reads and clears the device-side error word of the current device, after synchronising it.
- * The encoder sets bit 1 (value 1) when a TMA bulk copy does not complete within its bounded
- * wait; the affected tiles are then left unwritten.  *code_out = 0 means no such event.
+/* Bytes of device workspace kvarn_append_tokens needs: staging for B*Hkv K and V blocks
+ * (2 x 32 KiB each), their pool slots and a counter.  0 for an invalid shape. */
+size_t kvarn_append_workspace_size(int B, int Hkv);
+
+/* Commit the first n_accept[b] of n_new offered tokens of each sequence to its cache
+ * [paperlayer, "D Experimental details": a quantised body of 128-token blocks and unquantised
+ * trailing tokens; agihunt, pipeline paragraph: a block is quantised once it is done].  The
+ * accepted tokens go to the bf16 tail; a block they complete (128 tokens, or with
+ * KVARN_FLAG_FULL_TAIL a full tail followed by a newer token) is encoded with cfg into the pool
+ * slot block_table[b][h][block index] -- the same codes kvarn_encode_blocks gives for that
+ * block -- and the tail keeps the remaining tokens.  seq_lens[b] grows by the accepted count.
+ *   k_new_bf16, v_new_bf16 : [B][Hkv][n_new][128] bfloat16, original basis (post-RoPE K); n_new
+ *                 1..128 tokens offered per sequence this step.
+ *   n_accept    : [B] int32 device, tokens to commit (clamped to 0..n_new); NULL = all n_new
+ *                 (speculative decoding commits only the accepted prefix).
+ *   seq_lens    : [B] int32 device, updated in place.
+ *   k_tail_bf16, v_tail_bf16 : [B][Hkv][128][128] bfloat16 tails, updated in place.
+ *   pools, block_table, max_tiles : as for kvarn_decode_attention; written slots only.
+ *   workspace   : >= kvarn_append_workspace_size(B, Hkv) bytes, 256-byte aligned.
+ * A sequence whose completed block has no entry in the block table (index >= max_tiles) is left
+ * unchanged and bit 3 (value 4) of kvarn_device_error is set.  Host-side errors as elsewhere;
+ * nothing is enqueued on error.  Launches: one append kernel and two encode kernels. */
+kvarn_status kvarn_append_tokens(const kvarn_config* cfg, int B, int Hkv, const void* k_new_bf16,
+                                 const void* v_new_bf16, int n_new, const int32_t* n_accept,
+                                 int32_t* seq_lens, void* k_tail_bf16, void* v_tail_bf16, void* k_codes,
+                                 void* k_params, float* k_scale, void* v_codes, void* v_params,
+                                 float* v_scale, const int32_t* block_table, int max_tiles, void* workspace,
+                                 size_t workspace_bytes, kvarn_stream_t stream);
+
+/* Reads and clears the device-side error words of the current device, after synchronising it.
+ * Bit 1 (value 1): an encoder TMA bulk copy did not complete within its bounded wait (the affected
+ * tiles are left unwritten).  Bit 2 (value 2): a decode wait gave up.  Bit 3 (value 4): an append
+ * found no block-table slot for a completed block.  *code_out = 0 means no such event.
  * (A library diagnostic; the pages have no counterpart.) */
 kvarn_status kvarn_device_error(uint32_t* code_out);
 

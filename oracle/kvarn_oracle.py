@@ -492,3 +492,47 @@ def token_scale_ratio(x: np.ndarray, x_hat: np.ndarray) -> np.ndarray:
     n = np.linalg.norm(np.asarray(x, dtype=np.float64), axis=1)
     nh = np.linalg.norm(np.asarray(x_hat, dtype=np.float64), axis=1)
     return np.where(n > 0, nh / np.where(n > 0, n, 1.0), 1.0)
+
+
+# ----------------------------------------------------------------------------------------------
+# Appending tokens to the cache
+# ----------------------------------------------------------------------------------------------
+def append_tokens(k_new, v_new, n_accept, seq_lens, k_tail, v_tail, block_table, full_tail=False):
+    """Commit the first n_accept[b] of the offered tokens of each sequence to its cache.
+
+    The newest tokens stay unquantised in the tail; a 128-token block is quantised once it is
+    complete ([paperlayer] "D Experimental details": quantised body, FP16 trailing tokens;
+    [agihunt] pipeline paragraph: a block is quantised once it is done).  With the default
+    convention a block is complete when it holds 128 tokens; with full_tail it stays in the tail
+    until a newer token arrives (the full FP16 window of 1..128 tokens).  Only accepted tokens are
+    committed (speculative decoding keeps the rest out of the cache).
+    k_new, v_new: [B, hkv, n_new, 128]; tails: [B, hkv, 128, 128] (updated copies returned).
+    Returns (seq_lens', k_tail', v_tail', blocks) with blocks a list of (b, kv head, pool tile id,
+    k_block [128, 128], v_block [128, 128]) -- the blocks to encode into the pools."""
+    k_tail, v_tail = np.array(k_tail, copy=True), np.array(v_tail, copy=True)
+    lens = np.array(seq_lens, dtype=np.int64, copy=True)
+    blocks = []
+    bsz, hkv, n_new = k_new.shape[0], k_new.shape[1], k_new.shape[2]
+    for b in range(bsz):
+        a = int(min(max(int(n_accept[b]), 0), n_new))
+        length = int(lens[b])
+        if full_tail:
+            t0 = ((length - 1) % TILE) + 1 if length > 0 else 0
+            blk = (length - 1) // TILE if length > 0 else 0
+            complete = t0 + a > TILE
+        else:
+            t0, blk = length % TILE, length // TILE
+            complete = t0 + a >= TILE
+        need = TILE - t0 if complete else a
+        for h in range(hkv):
+            if complete:
+                kb = np.concatenate([k_tail[b, h, :t0], k_new[b, h, :need]], axis=0)
+                vb = np.concatenate([v_tail[b, h, :t0], v_new[b, h, :need]], axis=0)
+                blocks.append((b, h, int(block_table[b, h, blk]), kb, vb))
+                k_tail[b, h, :a - need] = k_new[b, h, need:a]
+                v_tail[b, h, :a - need] = v_new[b, h, need:a]
+            else:
+                k_tail[b, h, t0:t0 + a] = k_new[b, h, :a]
+                v_tail[b, h, t0:t0 + a] = v_new[b, h, :a]
+        lens[b] = length + a
+    return lens, k_tail, v_tail, blocks

@@ -178,3 +178,21 @@ def test_workspace_plan(lib):
     assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == expected(4, 40, 1024)
     assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == expected(1, 4, 0)
     assert kv.kvarn_decode_workspace_size(cfg, 1, 6, 4, 1) == 0
+
+
+def test_append_validation_needs_no_gpu(lib):
+    cfg = _cfg()
+
+    def call(B=2, Hkv=2, n_new=4, ws_bytes=1 << 30, ws=FAKE, seq=FAKE, max_tiles=4):
+        return lib.kvarn_append_tokens(ctypes.byref(cfg), B, Hkv, FAKE, FAKE, n_new, None, seq, FAKE, FAKE,
+                                       FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, max_tiles, ws, ws_bytes, None)
+
+    assert call(n_new=0) == 1 and call(n_new=129) == 1
+    assert call(Hkv=0) == 1 and call(B=-1) == 1 and call(max_tiles=-1) == 1
+    assert call(seq=None) == 1
+    assert b"seq_lens" in lib.kvarn_last_error()
+    assert call(ws=FAKE + 16) == 1  # the workspace must be 256-byte aligned
+    assert call(ws_bytes=100) == 4
+    assert call(B=0) == 0
+    assert lib.kvarn_append_workspace_size(2, 2) >= 2 * 4 * 32768
+    assert lib.kvarn_append_workspace_size(0, 0) == 0

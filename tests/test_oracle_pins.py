@@ -406,3 +406,43 @@ def test_decode_attention_with_sink_against_sdpa():
                 torch.from_numpy(q[b, h])[None, None, None], torch.from_numpy(kk)[None, None],
                 torch.from_numpy(vv)[None, None], scale=0.1)[0, 0, 0].numpy()
             assert np.abs(out[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("full_tail", [False, True])
+def test_append_tokens_rebuilds_the_same_cache_as_one_shot(full_tail):
+    # appending a token stream in random chunks gives the same tails and the same completed blocks
+    # as cutting the whole stream at once
+    rng = np.random.default_rng(60)
+    total, hkv = 700, 2
+    stream_k = rng.standard_normal((1, hkv, total, 128))
+    stream_v = rng.standard_normal((1, hkv, total, 128))
+    table = np.arange(8 * hkv).reshape(1, hkv, 8)
+    lens = np.array([0])
+    kt, vt = np.zeros((1, hkv, 128, 128)), np.zeros((1, hkv, 128, 128))
+    got_blocks = {}
+    pos = 0
+    while pos < total:
+        n_new = int(rng.integers(1, 129))
+        acc = int(rng.integers(0, n_new + 1))
+        acc = min(acc, total - pos)
+        kn = np.zeros((1, hkv, n_new, 128))
+        vn = np.zeros((1, hkv, n_new, 128))
+        kn[:, :, :acc] = stream_k[:, :, pos:pos + acc]
+        vn[:, :, :acc] = stream_v[:, :, pos:pos + acc]
+        kn[:, :, acc:] = 1e9  # offered but rejected tokens must never enter the cache
+        lens, kt, vt, blocks = o.append_tokens(kn, vn, [acc], lens, kt, vt, table, full_tail)
+        for b, h, tile, kb, vb in blocks:
+            assert tile not in got_blocks
+            got_blocks[tile] = (kb, vb)
+        pos += acc
+    assert lens[0] == total
+    n_full = ((total - 1) // 128 if full_tail else total // 128)
+    assert sorted(got_blocks) == sorted(int(table[0, h, i]) for h in range(hkv) for i in range(n_full))
+    for h in range(hkv):
+        for i in range(n_full):
+            kb, vb = got_blocks[int(table[0, h, i])]
+            assert np.array_equal(kb, stream_k[0, h, 128 * i:128 * (i + 1)])
+            assert np.array_equal(vb, stream_v[0, h, 128 * i:128 * (i + 1)])
+        tail = total - 128 * n_full
+        assert np.array_equal(kt[0, h, :tail], stream_k[0, h, 128 * n_full:])
+        assert np.array_equal(vt[0, h, :tail], stream_v[0, h, 128 * n_full:])
