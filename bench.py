@@ -237,6 +237,49 @@ def run_diagnostics():
                       "presets": res}), flush=True)
 
 
+def run_append_timing():
+    """Time kvarn_append_tokens on the decode workload's shape (B 16 x 8 kv heads): one token per
+    sequence per step (1 in 128 steps completes a block), and 128 tokens per sequence (every
+    sequence completes one block, as in chunked prefill)."""
+    import torch
+
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    kv.load()
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    dev = torch.device("cuda", 0)
+    B, H, mt = DEC_B, DEC_HKV, DEC_L // 128 + 2
+    n_tiles = B * H * mt
+    pools = [torch.zeros(n_tiles, 4096, dtype=torch.uint8, device=dev),
+             torch.zeros(n_tiles, 512, dtype=torch.uint8, device=dev), torch.zeros(n_tiles, device=dev),
+             torch.zeros(n_tiles, 4096, dtype=torch.uint8, device=dev),
+             torch.zeros(n_tiles, 512, dtype=torch.uint8, device=dev), torch.zeros(n_tiles, device=dev)]
+    table = torch.arange(n_tiles, dtype=torch.int32, device=dev).reshape(B, H, mt)
+    kt = torch.zeros(B, H, 128, 128, dtype=torch.bfloat16, device=dev)
+    vt = torch.zeros_like(kt)
+    ws = torch.empty(kv.kvarn_append_workspace_size(B, H), dtype=torch.uint8, device=dev)
+    res = {}
+    for n_new in (1, 128):
+        kn = torch.randn(B, H, n_new, 128, device=dev).to(torch.bfloat16)
+        lens = torch.zeros(B, dtype=torch.int32, device=dev)
+        times = []
+        steps = 256 if n_new == 1 else 64
+        for i in range(steps):
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if int(lens.max()) + n_new > 128 * mt:
+                lens.zero_()
+            a.record()
+            kv.kvarn_append_tokens(cfg, kn, kn, lens, kt, vt, *pools, table, ws)
+            c.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(c) * 1000)
+        assert kv.kvarn_device_error() == 0
+        res[f"n_new={n_new}"] = {"mean_us": round(statistics.mean(times), 2),
+                                 "median_us": round(statistics.median(times), 2),
+                                 "max_us": round(max(times), 2), "steps": steps}
+    print(json.dumps({"impl": "append", "shape": f"B={B}, Hkv={H}, k2v2", "results": res}), flush=True)
+
+
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
@@ -458,6 +501,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ctx", type=int, default=32768, help="decode context (profiling runs only)")
+    ap.add_argument("--append-timing", action="store_true",
+                    help="time kvarn_append_tokens on the decode shape instead of the step")
     ap.add_argument("--diagnostics", action="store_true",
                     help="print the codec's error diagnostics on the encode workload instead of timing")
     ap.add_argument("--only", default="all", choices=["all", "encode", "decode"],
@@ -467,6 +512,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.diagnostics:
         run_diagnostics()
+    elif args.append_timing:
+        run_append_timing()
     elif args.impl == "reference":
         run_reference(args)
     else:
