@@ -221,6 +221,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, world, device):
+    """Per-rank timings -> their maximum over the ranks (every rank gets the result)."""
+    import torch
+    import torch.distributed as tdist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_us_per_step(step_ms_max, world):
+    """N replicas each finish one step within the max-over-ranks time: the whole job's time per
+    step is that time divided by N (weak scaling, replicas only)."""
+    return step_ms_max * 1000.0 / world
+
+
 def run_diagnostics():
     """E_M / E_D split and token-scale statistics of each preset on the encode workload."""
     import torch
@@ -396,10 +413,8 @@ def run_gpu(args):
     enc_ms = [a.elapsed_time(b) for a, b, _ in marks]
     dec_ms = [b.elapsed_time(c) for _, b, c in marks]
     step_ms = statistics.mean(e + d for e, d in zip(enc_ms, dec_ms))
-    t = torch.tensor([step_ms, statistics.mean(enc_ms), statistics.mean(dec_ms)], device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms, enc_ms_m, dec_ms_m = (float(x) for x in t)
+    step_ms, enc_ms_m, dec_ms_m = max_over_ranks([step_ms, statistics.mean(enc_ms), statistics.mean(dec_ms)],
+                                                 world, device)
 
     # end to end through host buffers: H2D of the new K/V blocks and queries, D2H of the output
     hk = ek.cpu().pin_memory()
@@ -431,10 +446,7 @@ def run_gpu(args):
         if s >= args.warmup:
             e2e.append(a.elapsed_time(c))
     e2e_ms = statistics.mean(e2e) if e2e else float("nan")
-    t = torch.tensor([e2e_ms], device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], world, device)
 
     if rank == 0:
         hbm, src = peaks()
@@ -446,8 +458,7 @@ def run_gpu(args):
         dec_alg = d_cache + d_q + d_out
         dec_gbs = dec_alg / (dec_ms_m * 1e-3) / 1e9
         traffic = ncu_traffic("kvarn_decode_attention")
-        # N replicas each do one step of work in the max-over-ranks time
-        value_us = step_ms * 1000 / world
+        value_us = job_us_per_step(step_ms, world)
         line = {
             "metric": METRIC, "value": round(value_us, 2), "unit": "us/step", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -474,7 +485,7 @@ def run_gpu(args):
                          "achieved": round(dec_gbs, 1), "peak": hbm, "peak_source": src,
                          "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
                          "traffic": traffic},
-            "e2e": {"value": round(e2e_ms * 1000 / world, 2), "unit": "us/step",
+            "e2e": {"value": round(job_us_per_step(e2e_ms, world), 2), "unit": "us/step",
                     "h2d_bytes_per_step": 2 * ek.numel() * 2 + q.numel() * 2,
                     "d2h_bytes_per_step": out.numel() * 4,
                     "schedule": "K/V upload on a copy stream during the decode; encode after it; "
