@@ -8,13 +8,15 @@
 // token/channel variance normalisation, then RTN; normalisation factors absorbed into the
 // group scale).
 //
-// Design (GB300): persistent grid, one CTA per SM; the bf16 tile (32 KB, contiguous) arrives by a
-// 1-D TMA bulk copy into a double-buffered shared-memory slot while the previous tile is being
-// processed.  The rotation is two register passes around one shared-memory transpose
+// Design (GB300): persistent grid, two CTAs per SM, so that one tile's barriers and dependent
+// chains overlap the other's work; the bf16 tile (32 KB, contiguous) arrives by a 1-D TMA bulk copy,
+// and the next tile's copy starts as soon as the first rotation pass has consumed the current one.
+// The rotation is two register passes around one shared-memory transpose
 // (H_128 = (H_8 x I_16)(I_8 x H_16)).  Each thread then owns 8 tokens x 8 channels of the rotated
-// tile, Y and Y^2 held as float2 pairs, so every statistics update of the Sinkhorn iteration is
-// one packed FFMA2 per element: token sums reduce over 16 lanes by shuffles, channel sums over
-// the two half-warps by a shuffle and over the 8 warps through shared memory.
+// tile Y (64 registers, channel pairs packed as float2): every statistics update of the Sinkhorn
+// iteration is p = Y a (FMUL2), sum += p (FADD2), sum of squares += p p (FFMA2) over two elements;
+// token sums reduce over 16 lanes by shuffles, channel sums over the two half-warps by a shuffle
+// and over the 8 warps through shared memory.
 #include <climits>
 #include <type_traits>
 
@@ -32,10 +34,14 @@ constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 
 struct EncodeSmem {
-    __nv_bfloat16 xs[2][kTile * kTile];    // TMA destination, double-buffered (64 KB)
-    float ys[kTile * kYStride];            // FWHT staging (72 KB)
-    float2 red[kWarps][4][32];             // cross-warp partial sums (8 KB)
-    float2 aa[kTile];                      // (1/c, 1/c^2) per channel
+    __nv_bfloat16 xs[kTile * kTile];       // TMA destination (32 KB)
+    union {
+        float ys[kTile * kYStride];        // FWHT staging (72 KB), dead after the second pass
+        struct {
+            float2 red[kWarps][4][32];     // cross-warp partial sums (8 KB)
+            alignas(16) uint32_t codes[kTile * 16];  // packed rows (up to 8 KB)
+        } late;
+    } u;
     float cinv[kTile];                     // inverse channel factor 1 / c
     float logf_[kTile];                    // log of the other-axis factor
     float grp_min[kTile];
@@ -47,8 +53,7 @@ struct EncodeSmem {
     float bred[kWarps];                    // block reductions
     float bcast[4];
     alignas(16) uint8_t params[KVARN_PARAM_BYTES];
-    alignas(16) uint32_t codes[kTile * 16];  // packed rows (up to 8 KB)
-    alignas(8) uint64_t bar[2];
+    alignas(8) uint64_t bar;
 };
 
 __device__ __forceinline__ float block_sum_128(EncodeSmem& sm, float v, int tid) {
@@ -70,6 +75,11 @@ __device__ __forceinline__ float block_max_128(EncodeSmem& sm, float v, int tid)
     return r;
 }
 
+// Element (token slot k, channel h + 16 i) of a thread's rotated tile held as channel pairs.
+__device__ __forceinline__ float& yel(float2 (&y)[8][4], int k, int i) {
+    return (i & 1) ? y[k][i >> 1].y : y[k][i >> 1].x;
+}
+
 // Power-of-two tile factor: largest S/g in (128, 256] unless |m|/g would pass 32768.
 __device__ __forceinline__ float tile_factor(float s_max, float m_max) {
     int e = INT_MIN;
@@ -78,429 +88,480 @@ __device__ __forceinline__ float tile_factor(float s_max, float m_max) {
     return e == INT_MIN ? 1.f : ldexpf(1.f, e);
 }
 
+// One tile in sm.xs (already arrived) -> codes, parameters and tile factor of output slot otile.
+// next: the tile this CTA encodes after it (its copy starts once sm.xs is consumed), or null.
 template <int BITS, int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
-encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ codes_out,
-              uint8_t* __restrict__ params_out, float* __restrict__ scale_out, int iters,
-              int rotate, int normalize, const int32_t* __restrict__ n_dev,
-              const int32_t* __restrict__ dest) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
+__device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16* next, uint8_t* __restrict__ codes_out,
+                                            uint8_t* __restrict__ params_out, float* __restrict__ scale_out,
+                                            int64_t otile, int iters, int rotate, int normalize) {
     constexpr int kLevels = (1 << BITS) - 1;
     constexpr uint32_t kTileBytes = kTile * kTile * 2;
-
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int h = lane & 15;                 // channel lane: channels h + 16 i
     const int tsub = lane >> 4;
     const int tg = 2 * warp + tsub;          // token group: tokens tg + 16 k
-    // optional device-side tile count (at most n_tiles) and output slots (dest[i] for input tile i)
-    if (n_dev != nullptr) n_tiles = min(n_tiles, (int64_t)max(*n_dev, 0));
+    const __nv_bfloat16* xs = sm.xs;
 
-    if (tid == 0) {
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
+    // ---- rotation pass 1: H_16 over channel bits 0..3, 16 contiguous channels per item ----
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = tid + kThreads * it;
+        const int t = idx >> 3, c = idx & 7;
+        float2 f[8];  // channels 16 c + 2 m, 16 c + 2 m + 1 in f[m]
+        {
+            // the two 16-byte halves are read in a lane-dependent order (bank-conflict free)
+            const int sw = (c >> 2) & 1;
+            const uint4 ra = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * sw);
+            const uint4 rb = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * (sw ^ 1));
+            const uint4 r0 = sw ? rb : ra, r1 = sw ? ra : rb;
+            const __nv_bfloat162* p0 = reinterpret_cast<const __nv_bfloat162*>(&r0);
+            const __nv_bfloat162* p1 = reinterpret_cast<const __nv_bfloat162*>(&r1);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                f[m] = __bfloat1622float2(p0[m]);
+                f[4 + m] = __bfloat1622float2(p1[m]);
+            }
+        }
+        if (rotate) fwht_pairs<8>(f);
+        float* dst = sm.u.ys + t * kYStride + 16 * c;
+        {
+            // 16-byte chunks stored in a lane-dependent rotation (bank-conflict free)
+            const int rot = (c >> 1) & 3;
+            float4 a0 = make_float4(f[0].x, f[0].y, f[1].x, f[1].y), a1 = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+            float4 a2 = make_float4(f[4].x, f[4].y, f[5].x, f[5].y), a3 = make_float4(f[6].x, f[6].y, f[7].x, f[7].y);
+            rotl4(a0, a1, a2, a3, rot);
+            *reinterpret_cast<float4*>(dst + 4 * ((0 + rot) & 3)) = a0;
+            *reinterpret_cast<float4*>(dst + 4 * ((1 + rot) & 3)) = a1;
+            *reinterpret_cast<float4*>(dst + 4 * ((2 + rot) & 3)) = a2;
+            *reinterpret_cast<float4*>(dst + 4 * ((3 + rot) & 3)) = a3;
+        }
+    }
+    __syncthreads();
+    // the bf16 slot is free again: prefetch this CTA's next tile into it
+    if (tid == 0 && next != nullptr) {
+        fence_proxy_async();
+        mbar_expect_tx(&sm.bar, kTileBytes);
+        bulk_g2s(sm.xs, next, kTileBytes, &sm.bar);
+    }
+
+    // ---- rotation pass 2: H_8 over channel bits 4..6; thread keeps Y ----
+    // Register slot k of a thread holds token tg + 16 (k ^ kown), kown = channel-lane bits 3..1
+    // as a 3-bit number: the partner lanes of the token reductions (h ^ 8, h ^ 4, h ^ 2) then
+    // hold each other's tokens in complementary slots, so every lane keeps and sends the same
+    // slots and no per-lane selection is needed; after the reduction lane h owns token kown.
+    const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
+    // y[k][m]: token slot k, channels h + 16 (2 m) (.x) and h + 16 (2 m + 1) (.y)
+    float2 y[8][4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int t = tg + 16 * (k ^ kown);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            y[k][q] = make_float2(sm.u.ys[t * kYStride + h + 32 * q], sm.u.ys[t * kYStride + h + 32 * q + 16]);
+        if (rotate) {
+            fwht_pairs<4>(y[k]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[k][q] = fmul2(y[k][q], make_float2(kInvSqrt128, kInvSqrt128));
+        }
+    }
+    // the staging area is reused for the reductions and the packed rows below
+    __syncthreads();
+
+    // ---- dual-axis variance normalisation ----
+    // token step:   r_t = std_j(Y_tj / c_j)   (lane owns token kown of its 8 for the update)
+    // channel step: c_j = std_t(Y_tj / r_t)
+    // The factors are kept as their inverses b = 1/r, a = 1/c (one rsqrt each).
+    float b_own = 1.f;
+    float2 a2[4];  // (a, a) of channels h + 16 (2 m), h + 16 (2 m + 1)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a2[m] = make_float2(1.f, 1.f);
+    if (tid < kTile) sm.cinv[tid] = 1.f;
+    const int n_it = normalize ? iters : 0;
+    for (int itn = 0; itn < n_it; ++itn) {
+        // token step: acc[k] = (sum_j Y a, sum_j (Y a)^2) over this thread's channels
+        float2 acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float2 p = fmul2(y[k][0], a2[0]);
+            float2 s1 = p, s2 = fmul2(p, p);
+#pragma unroll
+            for (int m = 1; m < 4; ++m) {
+                p = fmul2(y[k][m], a2[m]);
+                s1 = fadd2(s1, p);
+                s2 = ffma2(p, p, s2);
+            }
+            acc[k] = make_float2(s1.x + s1.y, s2.x + s2.y);
+        }
+        // transposing reduction over the 16 channel lanes
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 send = acc[q + 4];
+            float2 keep = acc[q];
+            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 8),
+                                                   __shfl_xor_sync(0xffffffffu, send.y, 8)));
+            acc[q] = keep;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float2 send = acc[q + 2];
+            float2 keep = acc[q];
+            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
+                                                   __shfl_xor_sync(0xffffffffu, send.y, 4)));
+            acc[q] = keep;
+        }
+        {
+            const float2 send = acc[1];
+            float2 keep = acc[0];
+            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 2),
+                                                   __shfl_xor_sync(0xffffffffu, send.y, 2)));
+            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, keep.x, 1),
+                                                   __shfl_xor_sync(0xffffffffu, keep.y, 1)));
+            const float mean = keep.x * (1.f / kTile);
+            const float ms = keep.y * (1.f / kTile);
+            const float var = ms - mean * mean;
+            if (var > kDegenerateRel * ms) b_own = rsqrtf(var);
+        }
+        float2 bb[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int kt = k ^ kown;  // the lane owning slot k's token has kown == kt
+            const int src = (lane & 16) | (((kt >> 2) & 1) << 3) | (((kt >> 1) & 1) << 2) | ((kt & 1) << 1);
+            const float b = __shfl_sync(0xffffffffu, b_own, src);
+            bb[k] = make_float2(b, b);
+        }
+        // channel step: acc[i] = (sum_t Y b, sum_t (Y b)^2) for channel h + 16 i
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            float2 p = fmul2(y[0][m], bb[0]);
+            float2 s1 = p, s2 = fmul2(p, p);
+#pragma unroll
+            for (int k = 1; k < 8; ++k) {
+                p = fmul2(y[k][m], bb[k]);
+                s1 = fadd2(s1, p);
+                s2 = ffma2(p, p, s2);
+            }
+            acc[2 * m] = make_float2(s1.x, s2.x);
+            acc[2 * m + 1] = make_float2(s1.y, s2.y);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float2 send = tsub ? acc[q] : acc[q + 4];
+            float2 keep = tsub ? acc[q + 4] : acc[q];
+            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 16),
+                                                   __shfl_xor_sync(0xffffffffu, send.y, 16)));
+            sm.u.late.red[warp][q][lane] = keep;  // channel h + 16 (q + 4 tsub)
+        }
+        __syncthreads();
+        if (tid < kTile) {
+            const int j = tid, hj = j & 15, ij = j >> 4;
+            const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
+            float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                s = fadd2(s, sm.u.late.red[w][q][src_lane]);
+            }
+            const float mean = s.x * (1.f / kTile);
+            const float ms = s.y * (1.f / kTile);
+            const float var = ms - mean * mean;
+            float a = sm.cinv[j];
+            if (var > kDegenerateRel * ms) a = rsqrtf(var);
+            sm.cinv[j] = a;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) a2[m] = make_float2(sm.cinv[h + 32 * m], sm.cinv[h + 32 * m + 16]);
+    }
+
+    // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
+    // K: other axis = token (factor r); V: other axis = channel (factor c).
+    if (KIND == KVARN_KIND_K) {
+        if ((h & 1) == 0) sm.logf_[tg + 16 * kown] = -logf(b_own);
+    } else {
+        if (tid < kTile) sm.logf_[tid] = -logf(sm.cinv[tid]);
+    }
+    __syncthreads();
+    const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[tid] : 0.f, tid) * (1.f / kTile);
+    if (tid < kTile) {
+        float s2 = e4m3_value(e4m3_rn(expf(sm.logf_[tid] - mean_log)));
+        s2 = fminf(fmaxf(s2, 0.001953125f), 448.f);  // [2^-9, 448]
+        sm.params[128 + tid] = e4m3_rn(s2);
+        sm.oth_inv_s2[tid] = 1.f / s2;
+    }
+    __syncthreads();
+
+    // W = Y / s2, then per-group min / max
+    float gmin_own = 0.f, gmax_own = 0.f;  // V: this lane's token kown
+    if (KIND == KVARN_KIND_K) {
+        float2 mm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float inv = sm.oth_inv_s2[tg + 16 * (k ^ kown)];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) y[k][m] = fmul2(y[k][m], make_float2(inv, inv));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float lo = yel(y, 0, i), hi = lo;
+#pragma unroll
+            for (int k = 1; k < 8; ++k) {
+                lo = fminf(lo, yel(y, k, i));
+                hi = fmaxf(hi, yel(y, k, i));
+            }
+            mm[i] = make_float2(lo, hi);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float2 send = tsub ? mm[q] : mm[q + 4];
+            float2 keep = tsub ? mm[q + 4] : mm[q];
+            keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 16));
+            keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 16));
+            sm.u.late.red[warp][q][lane] = keep;
+        }
+        __syncthreads();
+        if (tid < kTile) {
+            const int j = tid, hj = j & 15, ij = j >> 4;
+            const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
+            float lo = sm.u.late.red[0][q][src_lane].x, hi = sm.u.late.red[0][q][src_lane].y;
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) {
+                lo = fminf(lo, sm.u.late.red[w][q][src_lane].x);
+                hi = fmaxf(hi, sm.u.late.red[w][q][src_lane].y);
+            }
+            sm.grp_min[j] = lo;
+            sm.grp_scale[j] = (hi - lo) / (float)kLevels;
+        }
+    } else {
+        float inv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) inv[i] = sm.oth_inv_s2[h + 16 * i];
+        float2 mm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float lo = 0.f, hi = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) y[k][m] = fmul2(y[k][m], make_float2(inv[2 * m], inv[2 * m + 1]));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float w = yel(y, k, i);
+                lo = i ? fminf(lo, w) : w;
+                hi = i ? fmaxf(hi, w) : w;
+            }
+            mm[k] = make_float2(lo, hi);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 send = mm[q + 4];
+            float2 keep = mm[q];
+            keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 8));
+            keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 8));
+            mm[q] = keep;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float2 send = mm[q + 2];
+            float2 keep = mm[q];
+            keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 4));
+            keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 4));
+            mm[q] = keep;
+        }
+        {
+            const float2 send = mm[1];
+            float2 keep = mm[0];
+            keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 2));
+            keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 2));
+            keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, keep.x, 1));
+            keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, keep.y, 1));
+            gmin_own = keep.x;
+            gmax_own = keep.y;
+        }
+        if ((h & 1) == 0) {
+            const int t = tg + 16 * kown;
+            sm.grp_min[t] = gmin_own;
+            sm.grp_scale[t] = (gmax_own - gmin_own) / (float)kLevels;
+        }
+    }
+    __syncthreads();
+
+    // ---- tile factor g, group scale S1 (E4M3, rounded up) and zero-point Z (FP16) ----
+    const float s_max = block_max_128(sm, tid < kTile ? sm.grp_scale[tid] : 0.f, tid);
+    const float m_max = block_max_128(sm, tid < kTile ? fabsf(sm.grp_min[tid]) : 0.f, tid);
+    const float g = tile_factor(s_max, m_max);
+    const float inv_g = 1.f / g;  // exact: g is a power of two
+    if (tid < kTile) {
+        const uint8_t s1b = e4m3_up(sm.grp_scale[tid] * inv_g);
+        const float s1 = e4m3_value(s1b);
+        const __half zh = __float2half_rn(sm.grp_min[tid] * inv_g);
+        sm.params[tid] = s1b;
+        reinterpret_cast<__half*>(sm.params + 256)[tid] = zh;
+        sm.grp_z[tid] = __half2float(zh);
+        sm.grp_inv_s1[tid] = s1 > 0.f ? 1.f / s1 : 0.f;
+        sm.grp_s1[tid] = s1;
+    }
+    __syncthreads();
+
+    // ---- codes and packing ----
+    // K rows are tokens: lane h of row t holds channels h + 16 i at bits BITS*i.
+    // V rows are channels: lane tg of row j holds tokens tg + 16 k at bits BITS*k.
+    uint32_t packed[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) packed[q] = 0;
+    {
+        // group constants: K groups are this thread's 8 channels, V groups its 8 tokens
+        float nz[8], is1[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * m) : (tg + 16 * (m ^ kown));
+            nz[m] = -sm.grp_z[grp];
+            is1[m] = sm.grp_inv_s1[grp];
+        }
+        // Adding 1.5 * 2^23 rounds a value in [0, 2^22) to an integer (half to even) held in the
+        // low mantissa bits.  Exact half-way points occur in practice only without the rotation
+        // (bf16 inputs on a coarse grid); there a product with the rounded reciprocal can land
+        // on the wrong side, so near a half-way point the code is redone with a correctly
+        // rounded division.  With the rotation the check is left out.
+        constexpr float kRound = 12582912.f;
+        auto quantise = [&](auto tie_check) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const int g0 = (KIND == KVARN_KIND_K) ? i : k, g1 = (KIND == KVARN_KIND_K) ? i + 1 : k;
+                    const float2 d = ffma2(y[k][i >> 1], make_float2(inv_g, inv_g),
+                                           make_float2(nz[g0], nz[g1]));
+                    const float2 u = fmul2(d, make_float2(is1[g0], is1[g1]));
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int ii = i + e, ge = e ? g1 : g0;
+                        const float ue = e ? u.y : u.x;
+                        float v = fminf(fmaxf(ue, 0.f), (float)kLevels);
+                        float r = v + kRound;
+                        if (decltype(tie_check)::value) {
+                            if (fabsf(v - (r - kRound)) > 0.4999f && is1[ge] > 0.f) {
+                                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * (k ^ kown));
+                                v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[grp]), 0.f), (float)kLevels);
+                                r = v + kRound;
+                            }
+                        }
+                        const uint32_t c = __float_as_uint(r) & (uint32_t)kLevels;
+                        if (KIND == KVARN_KIND_K)
+                            packed[k] |= c << (BITS * ii);
+                        else
+                            packed[ii] |= c << (BITS * (k ^ kown));
+                    }
+                }
+            }
+        };
+        if (rotate)
+            quantise(std::integral_constant<bool, false>());
+        else
+            quantise(std::integral_constant<bool, true>());
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int row = (KIND == KVARN_KIND_K) ? (tg + 16 * (q ^ kown)) : (h + 16 * q);
+        const int lane16 = (KIND == KVARN_KIND_K) ? h : tg;
+        if (BITS == 2)
+            reinterpret_cast<uint16_t*>(sm.u.late.codes)[row * 16 + lane16] = (uint16_t)packed[q];
+        else
+            sm.u.late.codes[row * 16 + lane16] = packed[q];
+    }
+    __syncthreads();
+
+    // ---- write out: codes (16-byte stores), params, tile factor ----
+    {
+        constexpr int kCodeBytes = kTile * 16 * BITS;
+        uint4* dst = reinterpret_cast<uint4*>(codes_out + otile * kCodeBytes);
+        const uint4* src = reinterpret_cast<const uint4*>(sm.u.late.codes);
+#pragma unroll
+        for (int v = tid; v < kCodeBytes / 16; v += kThreads) dst[v] = src[v];
+        if (tid < KVARN_PARAM_BYTES / 16)
+            reinterpret_cast<uint4*>(params_out + otile * KVARN_PARAM_BYTES)[tid] =
+                reinterpret_cast<const uint4*>(sm.params)[tid];
+        if (tid == 0) scale_out[otile] = g;
+    }
+    __syncthreads();
+}
+
+// Initialises the copy barrier and starts the copy of the CTA's first tile (if any).
+__device__ __forceinline__ void encode_prologue(EncodeSmem& sm, const __nv_bfloat16* first) {
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            int64_t t = blockIdx.x + (int64_t)b * gridDim.x;
-            if (t < n_tiles) {
-                mbar_expect_tx(&sm.bar[b], kTileBytes);
-                bulk_g2s(sm.xs[b], x + t * kTile * kTile, kTileBytes, &sm.bar[b]);
-            }
-        }
+    if (threadIdx.x == 0 && first != nullptr) {
+        mbar_expect_tx(&sm.bar, kTile * kTile * 2);
+        bulk_g2s(sm.xs, first, kTile * kTile * 2, &sm.bar);
     }
+}
 
+// Waits for the CTA's local-th tile.  False (uniform over the CTA) when its copy never arrived:
+// the error word is then set and the copy has been waited for (bounded).
+__device__ __forceinline__ bool encode_wait(EncodeSmem& sm, int local) {
+    const bool ok = mbar_wait(&sm.bar, local & 1, &g_encode_error);
+    if (__syncthreads_and(ok)) return true;
+    if (threadIdx.x == 0) mbar_drain(&sm.bar, local & 1);
+    return false;
+}
+
+// Tiles of one kind.  Optional device-side tile count n_dev (at most n_tiles) and output slots
+// (dest[i] for input tile i).
+template <int BITS, int KIND>
+__global__ void __launch_bounds__(kThreads, 2)
+encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ codes_out,
+              uint8_t* __restrict__ params_out, float* __restrict__ scale_out, int iters,
+              int rotate, int normalize, const int32_t* __restrict__ n_dev,
+              const int32_t* __restrict__ dest) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
+    if (n_dev != nullptr) n_tiles = min(n_tiles, (int64_t)max(*n_dev, 0));
+    encode_prologue(sm, blockIdx.x < n_tiles ? x + (int64_t)blockIdx.x * kTile * kTile : nullptr);
     int local = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
-        const int buf = local & 1;
-        const bool ok_data = mbar_wait(&sm.bar[buf], (local >> 1) & 1, &g_encode_error);
-        if (!__syncthreads_and(ok_data)) {
-            // a copy never arrived (the error word is set): wait for this CTA's copies, then stop
-            if (tid == 0) {
-                mbar_drain(&sm.bar[buf], (local >> 1) & 1);
-                if (tile + gridDim.x < n_tiles) mbar_drain(&sm.bar[buf ^ 1], ((local + 1) >> 1) & 1);
-            }
-            break;
-        }
-        const __nv_bfloat16* xs = sm.xs[buf];
+        if (!encode_wait(sm, local)) break;
+        const int64_t nt = tile + gridDim.x;
+        encode_tile<BITS, KIND>(sm, nt < n_tiles ? x + nt * kTile * kTile : nullptr, codes_out, params_out,
+                                scale_out, dest != nullptr ? (int64_t)dest[tile] : tile, iters, rotate, normalize);
+    }
+}
 
-        // ---- rotation pass 1: H_16 over channel bits 0..3, 16 contiguous channels per item ----
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int idx = tid + kThreads * it;
-            const int t = idx >> 3, c = idx & 7;
-            float2 f[8];  // channels 16 c + 2 m, 16 c + 2 m + 1 in f[m]
-            {
-                // the two 16-byte halves are read in a lane-dependent order (bank-conflict free)
-                const int sw = (c >> 2) & 1;
-                const uint4 ra = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * sw);
-                const uint4 rb = *reinterpret_cast<const uint4*>(xs + t * kTile + 16 * c + 8 * (sw ^ 1));
-                const uint4 r0 = sw ? rb : ra, r1 = sw ? ra : rb;
-                const __nv_bfloat162* p0 = reinterpret_cast<const __nv_bfloat162*>(&r0);
-                const __nv_bfloat162* p1 = reinterpret_cast<const __nv_bfloat162*>(&r1);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    f[m] = __bfloat1622float2(p0[m]);
-                    f[4 + m] = __bfloat1622float2(p1[m]);
-                }
-            }
-            if (rotate) fwht_pairs<8>(f);
-            float* dst = sm.ys + t * kYStride + 16 * c;
-            {
-                // 16-byte chunks stored in a lane-dependent rotation (bank-conflict free)
-                const int rot = (c >> 1) & 3;
-                float4 a0 = make_float4(f[0].x, f[0].y, f[1].x, f[1].y), a1 = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
-                float4 a2 = make_float4(f[4].x, f[4].y, f[5].x, f[5].y), a3 = make_float4(f[6].x, f[6].y, f[7].x, f[7].y);
-                rotl4(a0, a1, a2, a3, rot);
-                *reinterpret_cast<float4*>(dst + 4 * ((0 + rot) & 3)) = a0;
-                *reinterpret_cast<float4*>(dst + 4 * ((1 + rot) & 3)) = a1;
-                *reinterpret_cast<float4*>(dst + 4 * ((2 + rot) & 3)) = a2;
-                *reinterpret_cast<float4*>(dst + 4 * ((3 + rot) & 3)) = a3;
-            }
-        }
-        __syncthreads();
-        // the bf16 slot is free again: prefetch the tile after next into it
-        if (tid == 0) {
-            int64_t nt = tile + 2 * (int64_t)gridDim.x;
-            if (nt < n_tiles) {
-                fence_proxy_async();
-                mbar_expect_tx(&sm.bar[buf], kTileBytes);
-                bulk_g2s(sm.xs[buf], x + nt * kTile * kTile, kTileBytes, &sm.bar[buf]);
-            }
-        }
+// The K and V tiles of one call in one grid: virtual tile i < n_k is K tile i, else V tile i - n_k.
+struct EncodeKV {
+    const __nv_bfloat16* kx;
+    const __nv_bfloat16* vx;
+    int64_t n_k, n_v;
+    uint8_t* k_codes;
+    uint8_t* k_params;
+    float* k_scale;
+    uint8_t* v_codes;
+    uint8_t* v_params;
+    float* v_scale;
+    int iters, rotate, normalize;
+};
 
-        // ---- rotation pass 2: H_8 over channel bits 4..6; thread keeps (Y, Y^2) ----
-        // Register slot k of a thread holds token tg + 16 (k ^ kown), kown = channel-lane bits 3..1
-        // as a 3-bit number: the partner lanes of the token reductions (h ^ 8, h ^ 4, h ^ 2) then
-        // hold each other's tokens in complementary slots, so every lane keeps and sends the same
-        // slots and no per-lane selection is needed; after the reduction lane h owns token kown.
-        const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
-        float2 yy[8][8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int t = tg + 16 * (k ^ kown);
-            float2 f[4];  // channels h + 16 (2 q), h + 16 (2 q + 1) in f[q]
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                f[q] = make_float2(sm.ys[t * kYStride + h + 32 * q], sm.ys[t * kYStride + h + 32 * q + 16]);
-            if (rotate) {
-                fwht_pairs<4>(f);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) f[q] = fmul2(f[q], make_float2(kInvSqrt128, kInvSqrt128));
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 sq = fmul2(f[q], f[q]);
-                yy[k][2 * q] = make_float2(f[q].x, sq.x);
-                yy[k][2 * q + 1] = make_float2(f[q].y, sq.y);
-            }
-        }
+__device__ __forceinline__ const __nv_bfloat16* kv_src(const EncodeKV& a, int64_t i) {
+    return i < a.n_k ? a.kx + i * kTile * kTile : a.vx + (i - a.n_k) * kTile * kTile;
+}
 
-        // ---- dual-axis variance normalisation ----
-        // token step:   r_t = std_j(Y_tj / c_j)   (lane owns token kown of its 8 for the update)
-        // channel step: c_j = std_t(Y_tj / r_t)
-        // The factors are kept as their inverses b = 1/r, a = 1/c (one rsqrt each).
-        float b_own = 1.f;
-        float2 aa[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) aa[i] = make_float2(1.f, 1.f);
-        if (tid < kTile) sm.cinv[tid] = 1.f;
-        const int n_it = normalize ? iters : 0;
-        for (int itn = 0; itn < n_it; ++itn) {
-            // token step
-            float2 acc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                acc[k] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[k] = ffma2(yy[k][i], aa[i], acc[k]);
-            }
-            // transposing reduction over the 16 channel lanes
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 send = acc[q + 4];
-                float2 keep = acc[q];
-                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 8),
-                                                       __shfl_xor_sync(0xffffffffu, send.y, 8)));
-                acc[q] = keep;
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float2 send = acc[q + 2];
-                float2 keep = acc[q];
-                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
-                                                       __shfl_xor_sync(0xffffffffu, send.y, 4)));
-                acc[q] = keep;
-            }
-            {
-                const float2 send = acc[1];
-                float2 keep = acc[0];
-                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 2),
-                                                       __shfl_xor_sync(0xffffffffu, send.y, 2)));
-                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, keep.x, 1),
-                                                       __shfl_xor_sync(0xffffffffu, keep.y, 1)));
-                const float mean = keep.x * (1.f / kTile);
-                const float ms = keep.y * (1.f / kTile);
-                const float var = ms - mean * mean;
-                if (var > kDegenerateRel * ms) b_own = rsqrtf(var);
-            }
-            float2 bb[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int kt = k ^ kown;  // the lane owning slot k's token has kown == kt
-                const int src = (lane & 16) | (((kt >> 2) & 1) << 3) | (((kt >> 1) & 1) << 2) | ((kt & 1) << 1);
-                const float b = __shfl_sync(0xffffffffu, b_own, src);
-                bb[k] = make_float2(b, b * b);
-            }
-            // channel step
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) acc[i] = ffma2(yy[k][i], bb[k], acc[i]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float2 send = tsub ? acc[q] : acc[q + 4];
-                float2 keep = tsub ? acc[q + 4] : acc[q];
-                keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 16),
-                                                       __shfl_xor_sync(0xffffffffu, send.y, 16)));
-                sm.red[warp][q][lane] = keep;  // channel h + 16 (q + 4 tsub)
-            }
-            __syncthreads();
-            if (tid < kTile) {
-                const int j = tid, hj = j & 15, ij = j >> 4;
-                const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
-                float2 s = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    s = fadd2(s, sm.red[w][q][src_lane]);
-                }
-                const float mean = s.x * (1.f / kTile);
-                const float ms = s.y * (1.f / kTile);
-                const float var = ms - mean * mean;
-                float a = sm.cinv[j];
-                if (var > kDegenerateRel * ms) a = rsqrtf(var);
-                sm.cinv[j] = a;
-                sm.aa[j] = make_float2(a, a * a);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) aa[i] = sm.aa[h + 16 * i];
-        }
-
-        // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
-        // K: other axis = token (factor r); V: other axis = channel (factor c).
-        if (KIND == KVARN_KIND_K) {
-            if ((h & 1) == 0) sm.logf_[tg + 16 * kown] = -logf(b_own);
-        } else {
-            if (tid < kTile) sm.logf_[tid] = -logf(sm.cinv[tid]);
-        }
-        __syncthreads();
-        const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[tid] : 0.f, tid) * (1.f / kTile);
-        if (tid < kTile) {
-            float s2 = e4m3_value(e4m3_rn(expf(sm.logf_[tid] - mean_log)));
-            s2 = fminf(fmaxf(s2, 0.001953125f), 448.f);  // [2^-9, 448]
-            sm.params[128 + tid] = e4m3_rn(s2);
-            sm.oth_inv_s2[tid] = 1.f / s2;
-        }
-        __syncthreads();
-
-        // W = Y / s2, then per-group min / max
-        float gmin_own = 0.f, gmax_own = 0.f;  // V: this lane's token kown
-        if (KIND == KVARN_KIND_K) {
-            float2 mm[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float inv = sm.oth_inv_s2[tg + 16 * (k ^ kown)];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) yy[k][i].x *= inv;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float lo = yy[0][i].x, hi = yy[0][i].x;
-#pragma unroll
-                for (int k = 1; k < 8; ++k) {
-                    lo = fminf(lo, yy[k][i].x);
-                    hi = fmaxf(hi, yy[k][i].x);
-                }
-                mm[i] = make_float2(lo, hi);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float2 send = tsub ? mm[q] : mm[q + 4];
-                float2 keep = tsub ? mm[q + 4] : mm[q];
-                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 16));
-                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 16));
-                sm.red[warp][q][lane] = keep;
-            }
-            __syncthreads();
-            if (tid < kTile) {
-                const int j = tid, hj = j & 15, ij = j >> 4;
-                const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
-                float lo = sm.red[0][q][src_lane].x, hi = sm.red[0][q][src_lane].y;
-#pragma unroll
-                for (int w = 1; w < kWarps; ++w) {
-                    lo = fminf(lo, sm.red[w][q][src_lane].x);
-                    hi = fmaxf(hi, sm.red[w][q][src_lane].y);
-                }
-                sm.grp_min[j] = lo;
-                sm.grp_scale[j] = (hi - lo) / (float)kLevels;
-            }
-        } else {
-            float inv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) inv[i] = sm.oth_inv_s2[h + 16 * i];
-            float2 mm[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float lo = 0.f, hi = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float w = yy[k][i].x * inv[i];
-                    yy[k][i].x = w;
-                    lo = i ? fminf(lo, w) : w;
-                    hi = i ? fmaxf(hi, w) : w;
-                }
-                mm[k] = make_float2(lo, hi);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 send = mm[q + 4];
-                float2 keep = mm[q];
-                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 8));
-                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 8));
-                mm[q] = keep;
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float2 send = mm[q + 2];
-                float2 keep = mm[q];
-                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 4));
-                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 4));
-                mm[q] = keep;
-            }
-            {
-                const float2 send = mm[1];
-                float2 keep = mm[0];
-                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, send.x, 2));
-                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, send.y, 2));
-                keep.x = fminf(keep.x, __shfl_xor_sync(0xffffffffu, keep.x, 1));
-                keep.y = fmaxf(keep.y, __shfl_xor_sync(0xffffffffu, keep.y, 1));
-                gmin_own = keep.x;
-                gmax_own = keep.y;
-            }
-            if ((h & 1) == 0) {
-                const int t = tg + 16 * kown;
-                sm.grp_min[t] = gmin_own;
-                sm.grp_scale[t] = (gmax_own - gmin_own) / (float)kLevels;
-            }
-        }
-        __syncthreads();
-
-        // ---- tile factor g, group scale S1 (E4M3, rounded up) and zero-point Z (FP16) ----
-        const float s_max = block_max_128(sm, tid < kTile ? sm.grp_scale[tid] : 0.f, tid);
-        const float m_max = block_max_128(sm, tid < kTile ? fabsf(sm.grp_min[tid]) : 0.f, tid);
-        const float g = tile_factor(s_max, m_max);
-        const float inv_g = 1.f / g;  // exact: g is a power of two
-        if (tid < kTile) {
-            const uint8_t s1b = e4m3_up(sm.grp_scale[tid] * inv_g);
-            const float s1 = e4m3_value(s1b);
-            const __half zh = __float2half_rn(sm.grp_min[tid] * inv_g);
-            sm.params[tid] = s1b;
-            reinterpret_cast<__half*>(sm.params + 256)[tid] = zh;
-            sm.grp_z[tid] = __half2float(zh);
-            sm.grp_inv_s1[tid] = s1 > 0.f ? 1.f / s1 : 0.f;
-            sm.grp_s1[tid] = s1;
-        }
-        __syncthreads();
-
-        // ---- codes and packing ----
-        // K rows are tokens: lane h of row t holds channels h + 16 i at bits BITS*i.
-        // V rows are channels: lane tg of row j holds tokens tg + 16 k at bits BITS*k.
-        uint32_t packed[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) packed[q] = 0;
-        {
-            // group constants: K groups are this thread's 8 channels, V groups its 8 tokens
-            float nz[8], is1[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * m) : (tg + 16 * (m ^ kown));
-                nz[m] = -sm.grp_z[grp];
-                is1[m] = sm.grp_inv_s1[grp];
-            }
-            // Adding 1.5 * 2^23 rounds a value in [0, 2^22) to an integer (half to even) held in the
-            // low mantissa bits.  Exact half-way points occur in practice only without the rotation
-            // (bf16 inputs on a coarse grid); there a product with the rounded reciprocal can land
-            // on the wrong side, so near a half-way point the code is redone with a correctly
-            // rounded division.  With the rotation the check is left out.
-            constexpr float kRound = 12582912.f;
-            auto quantise = [&](auto tie_check) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-#pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const int g0 = (KIND == KVARN_KIND_K) ? i : k, g1 = (KIND == KVARN_KIND_K) ? i + 1 : k;
-                        const float2 d = ffma2(make_float2(yy[k][i].x, yy[k][i + 1].x), make_float2(inv_g, inv_g),
-                                               make_float2(nz[g0], nz[g1]));
-                        const float2 u = fmul2(d, make_float2(is1[g0], is1[g1]));
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int ii = i + e, ge = e ? g1 : g0;
-                            const float ue = e ? u.y : u.x;
-                            float v = fminf(fmaxf(ue, 0.f), (float)kLevels);
-                            float r = v + kRound;
-                            if (decltype(tie_check)::value) {
-                                if (fabsf(v - (r - kRound)) > 0.4999f && is1[ge] > 0.f) {
-                                    const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * (k ^ kown));
-                                    v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[grp]), 0.f), (float)kLevels);
-                                    r = v + kRound;
-                                }
-                            }
-                            const uint32_t c = __float_as_uint(r) & (uint32_t)kLevels;
-                            if (KIND == KVARN_KIND_K)
-                                packed[k] |= c << (BITS * ii);
-                            else
-                                packed[ii] |= c << (BITS * (k ^ kown));
-                        }
-                    }
-                }
-            };
-            if (rotate)
-                quantise(std::integral_constant<bool, false>());
-            else
-                quantise(std::integral_constant<bool, true>());
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int row = (KIND == KVARN_KIND_K) ? (tg + 16 * (q ^ kown)) : (h + 16 * q);
-            const int lane16 = (KIND == KVARN_KIND_K) ? h : tg;
-            if (BITS == 2)
-                reinterpret_cast<uint16_t*>(sm.codes)[row * 16 + lane16] = (uint16_t)packed[q];
-            else
-                sm.codes[row * 16 + lane16] = packed[q];
-        }
-        __syncthreads();
-
-        // ---- write out: codes (16-byte stores), params, tile factor ----
-        if (ok_data) {
-            constexpr int kCodeBytes = kTile * 16 * BITS;
-            const int64_t otile = dest != nullptr ? (int64_t)dest[tile] : tile;
-            uint4* dst = reinterpret_cast<uint4*>(codes_out + otile * kCodeBytes);
-            const uint4* src = reinterpret_cast<const uint4*>(sm.codes);
-#pragma unroll
-            for (int v = tid; v < kCodeBytes / 16; v += kThreads) dst[v] = src[v];
-            if (tid < KVARN_PARAM_BYTES / 16)
-                reinterpret_cast<uint4*>(params_out + otile * KVARN_PARAM_BYTES)[tid] =
-                    reinterpret_cast<const uint4*>(sm.params)[tid];
-            if (tid == 0) scale_out[otile] = g;
-        }
-        __syncthreads();
+template <int KB, int VB>
+__global__ void __launch_bounds__(kThreads, 2) encode_kv_kernel(EncodeKV a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
+    const int64_t n = a.n_k + a.n_v;
+    encode_prologue(sm, blockIdx.x < n ? kv_src(a, blockIdx.x) : nullptr);
+    int local = 0;
+    for (int64_t tile = blockIdx.x; tile < n; tile += gridDim.x, ++local) {
+        if (!encode_wait(sm, local)) break;
+        const int64_t nt = tile + gridDim.x;
+        const __nv_bfloat16* next = nt < n ? kv_src(a, nt) : nullptr;
+        if (tile < a.n_k)
+            encode_tile<KB, KVARN_KIND_K>(sm, next, a.k_codes, a.k_params, a.k_scale, tile, a.iters, a.rotate,
+                                          a.normalize);
+        else
+            encode_tile<VB, KVARN_KIND_V>(sm, next, a.v_codes, a.v_params, a.v_scale, tile - a.n_k, a.iters,
+                                          a.rotate, a.normalize);
     }
 }
 
@@ -525,10 +586,12 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    const int grid = (int)(n_tiles < sms ? n_tiles : sms);
+    const int grid = (int)(n_tiles < 2 * sms ? n_tiles : 2 * sms);  // two CTAs per SM
     const size_t smem = sizeof(EncodeSmem);
     auto run = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         kern<<<grid, kThreads, smem, stream>>>(static_cast<const __nv_bfloat16*>(x), n_tiles,
                                                static_cast<uint8_t*>(codes),
@@ -542,21 +605,47 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
     return run(encode_kernel<4, KVARN_KIND_V>);
 }
 
-// K then V blocks of one call: two launches in stream order.  (Overlapping the two grids -- one
-// fused grid, or the V grid started early on the SMs the K grid leaves -- measured slower when the
-// inputs come from HBM rather than L2, so they run one after the other.)
+// K then V blocks of one call in one grid of two CTAs per SM: the K and V tiles share the waves,
+// so the last wave of the K tiles no longer leaves SMs idle before the V tiles start.
 cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_k, void* k_codes,
                              void* k_params, float* k_scale, const void* v_x, int64_t n_v, void* v_codes,
                              void* v_params, float* v_scale, int iters, int rotate, int normalize,
                              cudaStream_t stream) {
-    if (n_k > 0) {
-        cudaError_t e = launch_encode(k_bits, KVARN_KIND_K, k_x, n_k, k_codes, k_params, k_scale, iters, rotate,
-                                      normalize, stream);
+    if (n_k + n_v == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    const int64_t n = n_k + n_v;
+    const int grid = (int)(n < 2 * sms ? n : 2 * sms);
+    const size_t smem = sizeof(EncodeSmem);
+    EncodeKV a;
+    a.kx = static_cast<const __nv_bfloat16*>(k_x);
+    a.vx = static_cast<const __nv_bfloat16*>(v_x);
+    a.n_k = n_k;
+    a.n_v = n_v;
+    a.k_codes = static_cast<uint8_t*>(k_codes);
+    a.k_params = static_cast<uint8_t*>(k_params);
+    a.k_scale = k_scale;
+    a.v_codes = static_cast<uint8_t*>(v_codes);
+    a.v_params = static_cast<uint8_t*>(v_params);
+    a.v_scale = v_scale;
+    a.iters = iters;
+    a.rotate = rotate;
+    a.normalize = normalize;
+    auto run = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-    }
-    if (n_v == 0) return cudaSuccess;
-    return launch_encode(v_bits, KVARN_KIND_V, v_x, n_v, v_codes, v_params, v_scale, iters, rotate, normalize,
-                         stream);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kThreads, smem, stream>>>(a);
+        return cudaGetLastError();
+    };
+    if (k_bits == 2 && v_bits == 2) return run(encode_kv_kernel<2, 2>);
+    if (k_bits == 4 && v_bits == 2) return run(encode_kv_kernel<4, 2>);
+    if (k_bits == 2 && v_bits == 4) return run(encode_kv_kernel<2, 4>);
+    return run(encode_kv_kernel<4, 4>);
 }
 
 }  // namespace kvarn
