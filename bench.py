@@ -469,7 +469,7 @@ def run_gpu(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "encode": {"us": round(enc_ms_m * 1000, 2), "gbs_bf16_input": round(enc_in_gbs, 1),
                        "gbs_read_plus_write": round(enc_gbs, 1), "hbm_frac": round(enc_gbs / hbm, 4),
-                       "bytes_per_step": e_in + e_out, "launches_per_step": 2,
+                       "bytes_per_step": e_in + e_out, "launches_per_step": 1,
                        "alu_roofline": {
                            "bound": "alu", "unit": "TFLOP/s",
                            "achieved": round(enc_tflops, 2), "peak": round(FP32_PEAK_TFLOPS, 1),
