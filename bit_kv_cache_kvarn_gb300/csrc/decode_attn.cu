@@ -175,34 +175,19 @@ __device__ __forceinline__ void unpack_row_to_tmem(const uint32_t (&x)[4 * BITS]
     }
 }
 
-// Read this thread's packed row (BITS*16 bytes) from shared memory; the 16-byte pieces are read in
-// a thread-dependent rotation so a quarter-warp touches every bank once.
+// Read this thread's packed row (BITS*16 bytes) from shared memory.  Rows are 32 (2-bit) or 64
+// (4-bit) bytes apart, so a quarter-warp's 16-byte reads meet 2- or 4-way bank conflicts; taking
+// them is cheaper than reading in a lane-dependent order and putting the words back in place.
 template <int BITS>
 __device__ __forceinline__ void load_row(const uint8_t* base, int r, uint32_t (&x)[4 * BITS]) {
     const uint4* p = reinterpret_cast<const uint4*>(base + r * 16 * BITS);
-    if (BITS == 2) {
-        const int sw = (r >> 2) & 1;
-        const uint4 a = p[sw], b = p[sw ^ 1];
-        const uint4 u0 = sw ? b : a, u1 = sw ? a : b;
-        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-    } else {
-        const int rot = (r >> 1) & 3;
-        uint4 u[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) u[q] = p[(q + rot) & 3];
-        // u[q] holds piece (q + rot) & 3: rotate back
-        float4 f0 = *reinterpret_cast<float4*>(&u[0]), f1 = *reinterpret_cast<float4*>(&u[1]);
-        float4 f2 = *reinterpret_cast<float4*>(&u[2]), f3 = *reinterpret_cast<float4*>(&u[3]);
-        rotl4(f0, f1, f2, f3, (4 - rot) & 3);
-        const float4 f[4] = {f0, f1, f2, f3};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            x[4 * q] = __float_as_uint(f[q].x);
-            x[4 * q + 1] = __float_as_uint(f[q].y);
-            x[4 * q + 2] = __float_as_uint(f[q].z);
-            x[4 * q + 3] = __float_as_uint(f[q].w);
-        }
+    for (int q = 0; q < BITS; ++q) {
+        const uint4 u = p[q];
+        x[4 * q] = u.x;
+        x[4 * q + 1] = u.y;
+        x[4 * q + 2] = u.z;
+        x[4 * q + 3] = u.w;
     }
 }
 
@@ -213,12 +198,24 @@ __device__ __forceinline__ void store_b(uint8_t* b, int kk, const float (&x)[GH]
     uint32_t w[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) w[q] = 0u;
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-        const __half hi = __float2half_rn(x[h]);
-        const __half lo = __float2half_rn((x[h] - __half2float(hi)) * kLoScale);
+    if constexpr (GH == 1) {
+        const __half hi = __float2half_rn(x[0]);
+        const __half lo = __float2half_rn((x[0] - __half2float(hi)) * kLoScale);
         const __half2 v = __halves2half2(hi, lo);
-        w[h] = *reinterpret_cast<const uint32_t*>(&v);
+        w[0] = *reinterpret_cast<const uint32_t*>(&v);
+    } else {
+        // two values at a time: packed conversions and residuals, then (hi, lo) per value
+#pragma unroll
+        for (int h = 0; h < GH; h += 2) {
+            const float2 xv = make_float2(x[h], x[h + 1]);
+            const __half2 hi = __floats2half2_rn(xv.x, xv.y);
+            const float2 r = fmul2(ffma2(__half22float2(hi), make_float2(-1.f, -1.f), xv),
+                                   make_float2(kLoScale, kLoScale));
+            const __half2 lo = __floats2half2_rn(r.x, r.y);
+            const uint32_t hb = *reinterpret_cast<const uint32_t*>(&hi), lb = *reinterpret_cast<const uint32_t*>(&lo);
+            w[h] = __byte_perm(hb, lb, 0x5410);
+            w[h + 1] = __byte_perm(hb, lb, 0x7632);
+        }
     }
     *reinterpret_cast<uint4*>(b + b_off(0, kk)) = make_uint4(w[0], w[1], w[2], w[3]);
     if (GH > 4) *reinterpret_cast<uint4*>(b + b_off(8, kk)) = make_uint4(w[4], w[5], w[6], w[7]);
