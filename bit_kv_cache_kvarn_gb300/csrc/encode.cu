@@ -33,6 +33,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 
+constexpr int kPadded = kTile + kTile / 16;
+__host__ __device__ constexpr int pad(int i) { return i + (i >> 4); }
+
 struct EncodeSmem {
     __nv_bfloat16 xs[kTile * kTile];       // TMA destination (32 KB)
     union {
@@ -43,13 +46,15 @@ struct EncodeSmem {
         } late;
     } u;
     float cinv[kTile];                     // inverse channel factor 1 / c
-    float logf_[kTile];                    // log of the other-axis factor
-    float grp_min[kTile];
-    float grp_scale[kTile];
-    float grp_z[kTile];                    // zero-point (value of the FP16 code)
-    float grp_inv_s1[kTile];               // 1 / S1 (0 where S1 = 0)
-    float grp_s1[kTile];                   // S1
-    float oth_inv_s2[kTile];               // 1 / s2 along the other axis
+    // per-group and per-other-axis arrays, indexed through pad(): a half-warp reads the 8 tokens
+    // tg + 16 k of its lanes' slots, which pad() spreads over 8 banks
+    float logf_[kPadded];                  // log of the other-axis factor
+    float grp_min[kPadded];
+    float grp_scale[kPadded];
+    float grp_z[kPadded];                  // zero-point (value of the FP16 code)
+    float grp_inv_s1[kPadded];             // 1 / S1 (0 where S1 = 0)
+    float grp_s1[kPadded];                 // S1
+    float oth_inv_s2[kPadded];             // 1 / s2 along the other axis
     float bred[kWarps];                    // block reductions
     float bcast[4];
     alignas(16) uint8_t params[KVARN_PARAM_BYTES];
@@ -277,17 +282,17 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
     // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
     // K: other axis = token (factor r); V: other axis = channel (factor c).
     if (KIND == KVARN_KIND_K) {
-        if ((h & 1) == 0) sm.logf_[tg + 16 * kown] = -logf(b_own);
+        if ((h & 1) == 0) sm.logf_[pad(tg + 16 * kown)] = -logf(b_own);
     } else {
-        if (tid < kTile) sm.logf_[tid] = -logf(sm.cinv[tid]);
+        if (tid < kTile) sm.logf_[pad(tid)] = -logf(sm.cinv[tid]);
     }
     __syncthreads();
-    const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[tid] : 0.f, tid) * (1.f / kTile);
+    const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[pad(tid)] : 0.f, tid) * (1.f / kTile);
     if (tid < kTile) {
-        float s2 = e4m3_value(e4m3_rn(expf(sm.logf_[tid] - mean_log)));
+        float s2 = e4m3_value(e4m3_rn(expf(sm.logf_[pad(tid)] - mean_log)));
         s2 = fminf(fmaxf(s2, 0.001953125f), 448.f);  // [2^-9, 448]
         sm.params[128 + tid] = e4m3_rn(s2);
-        sm.oth_inv_s2[tid] = 1.f / s2;
+        sm.oth_inv_s2[pad(tid)] = 1.f / s2;
     }
     __syncthreads();
 
@@ -297,7 +302,7 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
         float2 mm[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float inv = sm.oth_inv_s2[tg + 16 * (k ^ kown)];
+            const float inv = sm.oth_inv_s2[pad(tg + 16 * (k ^ kown))];
 #pragma unroll
             for (int m = 0; m < 4; ++m) y[k][m] = fmul2(y[k][m], make_float2(inv, inv));
         }
@@ -329,13 +334,13 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
                 lo = fminf(lo, sm.u.late.red[w][q][src_lane].x);
                 hi = fmaxf(hi, sm.u.late.red[w][q][src_lane].y);
             }
-            sm.grp_min[j] = lo;
-            sm.grp_scale[j] = (hi - lo) / (float)kLevels;
+            sm.grp_min[pad(j)] = lo;
+            sm.grp_scale[pad(j)] = (hi - lo) / (float)kLevels;
         }
     } else {
         float inv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) inv[i] = sm.oth_inv_s2[h + 16 * i];
+        for (int i = 0; i < 8; ++i) inv[i] = sm.oth_inv_s2[pad(h + 16 * i)];
         float2 mm[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -378,26 +383,26 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
         }
         if ((h & 1) == 0) {
             const int t = tg + 16 * kown;
-            sm.grp_min[t] = gmin_own;
-            sm.grp_scale[t] = (gmax_own - gmin_own) / (float)kLevels;
+            sm.grp_min[pad(t)] = gmin_own;
+            sm.grp_scale[pad(t)] = (gmax_own - gmin_own) / (float)kLevels;
         }
     }
     __syncthreads();
 
     // ---- tile factor g, group scale S1 (E4M3, rounded up) and zero-point Z (FP16) ----
-    const float s_max = block_max_128(sm, tid < kTile ? sm.grp_scale[tid] : 0.f, tid);
-    const float m_max = block_max_128(sm, tid < kTile ? fabsf(sm.grp_min[tid]) : 0.f, tid);
+    const float s_max = block_max_128(sm, tid < kTile ? sm.grp_scale[pad(tid)] : 0.f, tid);
+    const float m_max = block_max_128(sm, tid < kTile ? fabsf(sm.grp_min[pad(tid)]) : 0.f, tid);
     const float g = tile_factor(s_max, m_max);
     const float inv_g = 1.f / g;  // exact: g is a power of two
     if (tid < kTile) {
-        const uint8_t s1b = e4m3_up(sm.grp_scale[tid] * inv_g);
+        const uint8_t s1b = e4m3_up(sm.grp_scale[pad(tid)] * inv_g);
         const float s1 = e4m3_value(s1b);
-        const __half zh = __float2half_rn(sm.grp_min[tid] * inv_g);
+        const __half zh = __float2half_rn(sm.grp_min[pad(tid)] * inv_g);
         sm.params[tid] = s1b;
         reinterpret_cast<__half*>(sm.params + 256)[tid] = zh;
-        sm.grp_z[tid] = __half2float(zh);
-        sm.grp_inv_s1[tid] = s1 > 0.f ? 1.f / s1 : 0.f;
-        sm.grp_s1[tid] = s1;
+        sm.grp_z[pad(tid)] = __half2float(zh);
+        sm.grp_inv_s1[pad(tid)] = s1 > 0.f ? 1.f / s1 : 0.f;
+        sm.grp_s1[pad(tid)] = s1;
     }
     __syncthreads();
 
@@ -413,8 +418,8 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * m) : (tg + 16 * (m ^ kown));
-            nz[m] = -sm.grp_z[grp];
-            is1[m] = sm.grp_inv_s1[grp];
+            nz[m] = -sm.grp_z[pad(grp)];
+            is1[m] = sm.grp_inv_s1[pad(grp)];
         }
         // Adding 1.5 * 2^23 rounds a value in [0, 2^22) to an integer (half to even) held in the
         // low mantissa bits.  Exact half-way points occur in practice only without the rotation
@@ -440,7 +445,7 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
                         if (decltype(tie_check)::value) {
                             if (fabsf(v - (r - kRound)) > 0.4999f && is1[ge] > 0.f) {
                                 const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * (k ^ kown));
-                                v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[grp]), 0.f), (float)kLevels);
+                                v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[pad(grp)]), 0.f), (float)kLevels);
                                 r = v + kRound;
                             }
                         }
