@@ -8,11 +8,12 @@
 //   K (groups = channels): s_t = s2_t g (sum_j q'_j S1_j code_tj + sum_j q'_j Z_j)
 //   V (groups = tokens):   o_j += g s2_j (sum_t p_t S1_t code_tj + sum_t p_t Z_t)
 //
-// Split kernel (5th-generation tensor cores).  The context of each (sequence, kv head) is cut into
-// items of 16 tiles; a CTA holds two warpgroup "workers", each processing a contiguous run of
-// items persistently.  Per tile, one thread of the worker brings the packed K/V codes and
-// parameters into a shared-memory ring with 1-D TMA bulk copies (mbarrier-tracked); then thread r
-// of the worker:
+// Split kernel (5th-generation tensor cores).  The full tiles of all (sequence, kv head) units form
+// one stream that every CTA cuts, from the sequence lengths, into equal contiguous pieces of >= 16
+// tiles; a CTA holds two warpgroup "workers", each processing its piece persistently.  Per tile,
+// lane 0 of each of the worker's four warps brings one of the tile's four blocks (K codes, V codes,
+// K parameters, V parameters) into a shared-memory ring with a 1-D TMA bulk copy (mbarrier-tracked);
+// then thread r of the worker:
 //   * masks K row r (token r) into fp16 subnormals (code * 2^shift * 2^-24, exact; no conversion)
 //     and stores them in TMEM as the MMA's A operand;
 //   * writes q'' = q' S1 2^-shift for channel r as fp16 hi/lo pieces into the B operand (shared
@@ -25,8 +26,9 @@
 // and whether or not they share an accumulator), while MMAs issued by different warps overlap.
 // So each of the worker's 4 warps issues 2 of the 8 K-steps into its own 16-column partial
 // accumulator and the partials are summed on readout; the zero-point sums stay on the CUDA cores.
-// Merge kernel: one warp per (sequence, query head) merges the items by log-sum-exp, applies the
-// inverse rotation, attends to the unquantised bf16 tail and normalises.
+// Merge kernel: one warp per (sequence, query head) merges the partial slots by log-sum-exp, applies
+// the inverse rotation, attends to the unquantised bf16 tail and normalises.  Two launches per call,
+// both with programmatic dependent launch.
 #include <math.h>
 
 #include "kvarn_common.cuh"
@@ -44,7 +46,6 @@ constexpr int kThreads = 256;
 constexpr int kWorkers = 2;                 // warpgroups per CTA
 constexpr int kTilesPerSplit = 16;         // one partial slot per 16-tile block of a unit (+1, below)
 constexpr int kMinPiece = 16;              // every worker's piece of the tile stream has >= 16 tiles
-constexpr int kMaxWorkers = 4096;          // plan entries reserved in the workspace
 constexpr int kIdRing = 32;                // tile-id ring of a worker
 constexpr int kIdBatch = 16;               // tile ids are fetched 16 at a time, one batch ahead
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
@@ -94,8 +95,6 @@ struct DecodeArgs {
     int units;      // units per sequence: kv heads x head blocks
     int hblocks;    // head blocks per kv head
     float* ws;
-    long long* prefix;          // [B + 1] exclusive prefix of full tiles per sequence
-    PlanEntry* plan;            // [workers]
     float* out;
 };
 
@@ -391,6 +390,92 @@ __device__ __forceinline__ float* slot_ptr(const DecodeArgs& a, int b, int hq, i
     return a.ws + (((size_t)b * a.Hq + hq) * (a.splits + 1) + k) * kWsStride;
 }
 
+// Sum of v over the CTA's kThreads threads (every thread gets it); scratch holds kThreads / 32 values.
+__device__ __forceinline__ long long cta_sum(long long v, long long* scratch) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    long long t = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) t += scratch[w];
+    return t;
+}
+
+// The pieces of this CTA's workers.  The stream of full tiles -- sequence by sequence, unit by unit
+// (unit = kv head x head block) -- is cut into w_used equal contiguous runs of >= kMinPiece tiles,
+// worker w taking run w (none when w >= w_used); this balances the grid to a tile whatever the
+// length mix.  Every CTA computes it from the lengths (two passes over the sequences).
+__device__ PlanEntry find_piece(const DecodeArgs& a, int wk, long long* scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    long long own = 0;
+    for (int b = tid; b < a.B; b += kThreads) own += full_tiles(a, b);
+    const long long units = a.units;
+    const long long total = units * cta_sum(own, scratch);
+    const long long n_workers = (long long)gridDim.x * kWorkers;
+    long long w_used = total / kMinPiece;
+    if (w_used < 1) w_used = total > 0 ? 1 : 0;
+    if (w_used > n_workers) w_used = n_workers;
+    long long g0[kWorkers];  // first stream tile of each of the CTA's workers (-1: no piece)
+#pragma unroll
+    for (int k = 0; k < kWorkers; ++k) {
+        const long long w = (long long)blockIdx.x * kWorkers + k;
+        g0[k] = w < w_used ? total * w / w_used : -1;
+    }
+    PlanEntry e;
+    e.b = e.u = e.j = e.pad = 0;
+    e.len = 0;
+    e.pad2 = 0;
+    const long long w = (long long)blockIdx.x * kWorkers + wk;
+    if (w < w_used) e.len = total * (w + 1) / w_used - total * w / w_used;
+    // the sequence holding tile g0 of the stream: exclusive prefix sums of the tiles per sequence
+    long long carry = 0;
+    __shared__ int s_b[kWorkers];
+    __shared__ long long s_rem[kWorkers];
+    if (tid < kWorkers) {
+        s_b[tid] = 0;
+        s_rem[tid] = 0;
+    }
+    for (int base = 0; base < a.B; base += kThreads) {
+        const int b = base + tid;
+        const long long v = b < a.B ? (long long)full_tiles(a, b) : 0;
+        long long inc = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += y;
+        }
+        __syncthreads();
+        if (lane == 31) scratch[warp] = inc;
+        __syncthreads();
+        long long before = 0, chunk = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            before += w < warp ? scratch[w] : 0;
+            chunk += scratch[w];
+        }
+        const long long pre = carry + before + inc - v;
+        if (v > 0) {
+#pragma unroll
+            for (int k = 0; k < kWorkers; ++k)
+                if (g0[k] >= units * pre && g0[k] < units * (pre + v)) {
+                    s_b[k] = b;
+                    s_rem[k] = g0[k] - units * pre;
+                }
+        }
+        carry += chunk;
+    }
+    __syncthreads();
+    if (e.len > 0) {
+        const long long nt = full_tiles(a, s_b[wk]);
+        e.b = s_b[wk];
+        e.u = (int)(s_rem[wk] / nt);
+        e.j = (int)(s_rem[wk] % nt);
+    }
+    return e;
+}
+
 template <int KB, int VB, int GH>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_split_kernel(DecodeArgs a) {
@@ -421,9 +506,8 @@ decode_split_kernel(DecodeArgs a) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmab + kWorkers);
 
     const int hblocks = a.hblocks;
-    const int worker = blockIdx.x * kWorkers + wk;
     // programmatic dependent launch: the merge grid may be scheduled early (it waits for this
-    // grid before reading the workspace); this grid's prologue overlaps the plan kernel's tail
+    // grid before reading the workspace); this grid's prologue overlaps the previous kernel's tail
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     for (int i = tid; i < (int)(kWorkers * 2 * kBBytes / 16); i += kThreads) {
@@ -437,8 +521,9 @@ decode_split_kernel(DecodeArgs a) {
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan kernel's results are visible
-    const PlanEntry piece = a.plan[worker];
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernels' writes are visible
+    __shared__ long long s_scratch[kThreads / 32];
+    const PlanEntry piece = find_piece(a, wk, s_scratch);
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const uint32_t a_col = tmem + 128 * wk, d_col = a_col + 64;  // D: 4 partials x 16 columns
@@ -835,75 +920,6 @@ decode_split_kernel(DecodeArgs a) {
     if (warp == 0) tc::dealloc(tmem, kTmemCols);
 }
 
-// One block of 1024 threads: prefix sums of the full tiles per sequence, then each worker's piece
-// of the tile stream -- equal shares of >= kMinPiece tiles, so the split kernel is balanced to a
-// tile whatever the length mix.
-__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a, int n_workers) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ long long warp_tot[32];
-    __shared__ long long carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) carry = 0;
-    __syncthreads();
-    for (int base = 0; base < a.B; base += 1024) {
-        const int b = base + tid;
-        const long long v = b < a.B ? (long long)full_tiles(a, b) : 0;
-        long long inc = v;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const long long y = __shfl_up_sync(0xffffffffu, inc, d);
-            if (lane >= d) inc += y;
-        }
-        if (lane == 31) warp_tot[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            long long t = warp_tot[lane], ti = t;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const long long y = __shfl_up_sync(0xffffffffu, ti, d);
-                if (lane >= d) ti += y;
-            }
-            warp_tot[lane] = ti - t;  // exclusive prefix of the warp totals
-        }
-        __syncthreads();
-        const long long c0 = carry;
-        if (b < a.B) a.prefix[b] = c0 + warp_tot[warp] + inc - v;
-        __syncthreads();
-        if (tid == 1023) carry = c0 + warp_tot[31] + inc;
-        __syncthreads();
-    }
-    if (tid == 0) a.prefix[a.B] = carry;
-    __syncthreads();
-    const long long units = a.units;
-    const long long total = units * carry;
-    long long w_used = total / kMinPiece;
-    if (w_used < 1) w_used = total > 0 ? 1 : 0;
-    if (w_used > n_workers) w_used = n_workers;
-    for (int w = tid; w < n_workers; w += 1024) {
-        PlanEntry e;
-        e.b = e.u = e.j = e.pad = 0;
-        e.len = 0;
-        e.pad2 = 0;
-        if (w < w_used) {
-            const long long g0 = total * w / w_used, g1 = total * (w + 1) / w_used;
-            // last sequence whose first tile is at or before g0 (it has full tiles)
-            int lo = 0, hi = a.B - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (units * a.prefix[mid] <= g0) lo = mid;
-                else hi = mid - 1;
-            }
-            const long long rem = g0 - units * a.prefix[lo];
-            const long long nt = a.prefix[lo + 1] - a.prefix[lo];
-            e.b = lo;
-            e.u = (int)(rem / nt);
-            e.j = (int)(rem % nt);
-            e.len = g1 - g0;
-        }
-        a.plan[w] = e;
-    }
-}
-
 // One warp per (sequence, query head): merge splits, inverse rotation, bf16 tail, normalise.
 __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     const int lane = threadIdx.x;
@@ -1015,13 +1031,16 @@ cudaError_t launch_dependent(Kern kern, dim3 grid, dim3 block, size_t smem, cuda
     return cudaLaunchKernelEx(&lc, kern, a);
 }
 
-int split_grid() {
+// Persistent grid: two CTAs per SM, or fewer when at most max_stream_tiles full tiles (an upper
+// bound the host knows: sequences x units x block-table width) cannot keep them all busy with pieces
+// of >= kMinPiece tiles.
+int split_grid(long long max_stream_tiles) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    int grid = 2 * sms;  // persistent: two CTAs per SM
-    if (grid * kWorkers > kMaxWorkers) grid = kMaxWorkers / kWorkers;
-    return grid;
+    const long long pieces = (max_stream_tiles + kMinPiece - 1) / kMinPiece;
+    const long long ctas = (pieces + kWorkers - 1) / kWorkers;
+    return (int)(ctas < 1 ? 1 : (ctas < 2 * sms ? ctas : 2 * sms));
 }
 
 template <int KB, int VB, int GH>
@@ -1043,16 +1062,12 @@ cudaError_t run_split_g(const DecodeArgs& a, int gh, int grid, cudaStream_t stre
 
 }  // namespace
 
-// Workspace: partial slots [B][Hq][splits + 1][132] f32 | prefix [B + 1] i64 | plan [4096] x 32 B,
-// each part 256-byte aligned.
+// Workspace: the partial slots [B][Hq][splits + 1][132] f32, rounded up to 256 bytes.
 DecodePlan plan_decode(int B, int Hq, int /*Hkv*/, int max_tiles) {
     DecodePlan p;
     p.tiles_per_split = kTilesPerSplit;
     p.splits = max_tiles <= 0 ? 1 : (max_tiles + kTilesPerSplit - 1) / kTilesPerSplit;
-    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    p.prefix_offset = up((size_t)B * Hq * (p.splits + 1) * kWsStride * sizeof(float));
-    p.plan_offset = p.prefix_offset + up((size_t)(B + 1) * sizeof(long long));
-    p.workspace_bytes = p.plan_offset + (size_t)kMaxWorkers * sizeof(PlanEntry);
+    p.workspace_bytes = ((size_t)B * Hq * (p.splits + 1) * kWsStride * sizeof(float) + 255) & ~(size_t)255;
     return p;
 }
 
@@ -1100,14 +1115,10 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.hblocks = group / gh;
     a.units = Hkv * a.hblocks;
     a.ws = static_cast<float*>(workspace);
-    a.prefix = reinterpret_cast<long long*>(static_cast<uint8_t*>(workspace) + plan.prefix_offset);
-    a.plan = reinterpret_cast<PlanEntry*>(static_cast<uint8_t*>(workspace) + plan.plan_offset);
     a.out = out;
-    const int grid = split_grid();
+    const int grid = split_grid((long long)B * a.units * (max_tiles > 0 ? max_tiles : 0));
     if (grid <= 0) return cudaErrorInvalidDevice;
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a, grid * kWorkers);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, grid, stream);
     else if (k_bits == 4 && v_bits == 2) e = run_split_g<4, 2>(a, gh, grid, stream);
     else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, grid, stream);

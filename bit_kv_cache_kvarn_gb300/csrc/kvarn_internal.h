@@ -27,12 +27,10 @@ cudaError_t launch_dequant(int bits, int kind, const void* codes, const void* pa
                            const float* tile_scale, int64_t n_tiles, int original_basis,
                            int rotate, float* out, cudaStream_t stream);
 
-// Split-K plan for decode attention: partial-slot granularity, slot count and workspace layout.
+// Split-K layout for decode attention: partial-slot granularity, slot count and workspace size.
 struct DecodePlan {
     int tiles_per_split;
     int splits;
-    size_t prefix_offset;  // byte offsets inside the workspace
-    size_t plan_offset;
     size_t workspace_bytes;
 };
 DecodePlan plan_decode(int B, int Hq, int Hkv, int max_tiles);

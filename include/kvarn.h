@@ -147,10 +147,9 @@ kvarn_status kvarn_dequant(const kvarn_config* cfg, kvarn_kind kind, const void*
                            const void* params, const float* tile_scale, int64_t n_tiles,
                            int original_basis, float* out, kvarn_stream_t stream);
 
-/* Bytes of device workspace kvarn_decode_attention needs for this shape, in three 256-byte
- * aligned parts: split-K partials [B][Hq][S + 1][132] float32 with S = ceil(max_tiles / 16)
- * (m, l, 2 pad, o[128] per slot), per-sequence tile prefix sums [B + 1] int64, and 4096 work
- * descriptors of 32 bytes.  Returns 0 for an invalid shape.  (The split-K decomposition and its
+/* Bytes of device workspace kvarn_decode_attention needs for this shape: the split-K partials
+ * [B][Hq][S + 1][132] float32 with S = ceil(max_tiles / 16) (m, l, 2 pad, o[128] per slot; S = 1
+ * when max_tiles is 0), rounded up to a multiple of 256.  Returns 0 for an invalid shape.  (The split-K decomposition and its
  * log-sum-exp merge are this library's; the pages only say that attention reads the cache.) */
 size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int Hkv,
                                    int max_tiles);

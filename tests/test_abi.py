@@ -168,11 +168,11 @@ def test_workspace_plan(lib):
     cfg = _cfg()
 
     def expected(B, Hq, max_tiles):
-        # partial slots: one per 16-tile block plus one; (m, l, 2 pad, o[128]) floats per slot;
-        # then int64 prefix sums [B + 1] and 4096 work descriptors of 32 bytes, 256-byte aligned
+        # partial slots: one per 16-tile block plus one; (m, l, 2 pad, o[128]) floats per slot,
+        # rounded up to 256 bytes
         up = lambda x: (x + 255) // 256 * 256
         slots = max(1, -(-max_tiles // 16)) + 1
-        return up(B * Hq * slots * 132 * 4) + up((B + 1) * 8) + 4096 * 32
+        return up(B * Hq * slots * 132 * 4)
 
     assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == expected(16, 32, 256)
     assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == expected(4, 40, 1024)
