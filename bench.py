@@ -254,6 +254,55 @@ def run_diagnostics():
                       "presets": res}), flush=True)
 
 
+def run_latency():
+    """Decode latency of single calls at serving-like shapes (32q/8kv heads, 2-bit K and V, full
+    tiles, no tail): back-to-back calls timed with CUDA events, cache re-read from L2 where it fits
+    (not flushed), so the numbers show the call's own latency, not HBM time."""
+    import torch
+
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    kv.load()
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    dev = torch.device("cuda", 0)
+    res = {}
+    for B, ctx in ((1, 4096), (1, 32768), (4, 8192), (16, 32768)):
+        nt = ctx // 128
+        n = B * DEC_HKV * nt
+        pool = min(n, 4096)  # distinct tiles; the block table cycles through them
+        g = torch.Generator(device="cpu").manual_seed(11)
+        x = torch.randn(pool, 128, 128, generator=g).to(torch.bfloat16).to(dev)
+        pk = (torch.empty(pool, 4096, dtype=torch.uint8, device=dev),
+              torch.empty(pool, 512, dtype=torch.uint8, device=dev), torch.empty(pool, device=dev))
+        pv = tuple(torch.empty_like(t) for t in pk)
+        kv.kvarn_encode_kv_blocks(cfg, x, x, *pk, *pv)
+        table = (torch.arange(n, dtype=torch.int32, device=dev) % pool).reshape(B, DEC_HKV, nt)
+        lens = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+        tail = torch.zeros(B, DEC_HKV, 128, 128, dtype=torch.bfloat16, device=dev)
+        q = torch.randn(B, DEC_HQ, 128, generator=g).to(torch.bfloat16).to(dev)
+        ws = torch.empty(kv.kvarn_decode_workspace_size(cfg, B, DEC_HQ, DEC_HKV, nt), dtype=torch.uint8, device=dev)
+        out = torch.empty(B, DEC_HQ, 128, device=dev)
+
+        def call():
+            kv.kvarn_decode_attention(cfg, q, DEC_HKV, *pk, *pv, table, lens, tail, tail, 1 / math.sqrt(128),
+                                      ws, out)
+
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 200
+        a.record()
+        for _ in range(reps):
+            call()
+        c.record()
+        torch.cuda.synchronize()
+        res[f"B={B}, ctx={ctx}"] = round(a.elapsed_time(c) / reps * 1000, 2)
+    assert kv.kvarn_device_error() == 0
+    print(json.dumps({"impl": "latency", "unit": "us per call", "heads": f"{DEC_HQ}q/{DEC_HKV}kv",
+                      "preset": "kvarn_k2v2_g128", "results": res}), flush=True)
+
+
 def run_append_timing():
     """Time kvarn_append_tokens on the decode workload's shape (B 16 x 8 kv heads): one token per
     sequence per step (1 in 128 steps completes a block), and 128 tokens per sequence (every
@@ -514,6 +563,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=32768, help="decode context (profiling runs only)")
     ap.add_argument("--append-timing", action="store_true",
                     help="time kvarn_append_tokens on the decode shape instead of the step")
+    ap.add_argument("--latency", action="store_true",
+                    help="time single decode calls at small serving shapes instead of the step")
     ap.add_argument("--diagnostics", action="store_true",
                     help="print the codec's error diagnostics on the encode workload instead of timing")
     ap.add_argument("--only", default="all", choices=["all", "encode", "decode"],
@@ -525,6 +576,8 @@ def main():
         run_diagnostics()
     elif args.append_timing:
         run_append_timing()
+    elif args.latency:
+        run_latency()
     elif args.impl == "reference":
         run_reference(args)
     else:

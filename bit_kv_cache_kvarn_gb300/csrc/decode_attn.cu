@@ -44,8 +44,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWorkers = 2;                 // warpgroups per CTA
-constexpr int kTilesPerSplit = 16;         // one partial slot per 16-tile block of a unit (+1, below)
-constexpr int kMinPiece = 16;              // every worker's piece of the tile stream has >= 16 tiles
+// Piece granularity P (DecodeArgs::piece): every worker's piece of the tile stream has >= P tiles and
+// a unit has one partial slot per P-tile block (+1, below).  P = 16 when the stream can fill the
+// GPU's workers with 16-tile pieces; smaller calls halve it (down to 2) so that more workers share
+// the tiles and the call's latency is not one worker walking 16 tiles.
+constexpr int kMaxPiece = 16, kMinPieceTiles = 2;
+constexpr long long kFillWorkers = 512;  // device-independent stand-in for the worker count
 constexpr int kIdRing = 32;                // tile-id ring of a worker
 constexpr int kIdBatch = 16;               // tile ids are fetched 16 at a time, one batch ahead
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
@@ -91,6 +95,7 @@ struct DecodeArgs {
     int rotate;
     int full_tail;  // the tail holds the last 1..128 tokens (else L mod 128)
     int splits;     // partial slots per (sequence, query head) = splits + 1
+    int piece;      // P: minimum piece length and tiles per partial slot block
     int B;
     int units;      // units per sequence: kv heads x head blocks
     int hblocks;    // head blocks per kv head
@@ -404,7 +409,7 @@ __device__ __forceinline__ long long cta_sum(long long v, long long* scratch) {
 }
 
 // The pieces of this CTA's workers.  The stream of full tiles -- sequence by sequence, unit by unit
-// (unit = kv head x head block) -- is cut into w_used equal contiguous runs of >= kMinPiece tiles,
+// (unit = kv head x head block) -- is cut into w_used equal contiguous runs of >= P tiles,
 // worker w taking run w (none when w >= w_used); this balances the grid to a tile whatever the
 // length mix.  Every CTA computes it from the lengths (two passes over the sequences).
 __device__ PlanEntry find_piece(const DecodeArgs& a, int wk, long long* scratch) {
@@ -414,7 +419,7 @@ __device__ PlanEntry find_piece(const DecodeArgs& a, int wk, long long* scratch)
     const long long units = a.units;
     const long long total = units * cta_sum(own, scratch);
     const long long n_workers = (long long)gridDim.x * kWorkers;
-    long long w_used = total / kMinPiece;
+    long long w_used = total / a.piece;
     if (w_used < 1) w_used = total > 0 ? 1 : 0;
     if (w_used > n_workers) w_used = n_workers;
     long long g0[kWorkers];  // first stream tile of each of the CTA's workers (-1: no piece)
@@ -853,7 +858,7 @@ decode_split_kernel(DecodeArgs a) {
         // ---- this segment's partial (m, l, o) for its heads ----
         // Slots of a unit: k < ceil(nt / 16) for the 16-tile block in which a piece starts, and
         // slot `splits` for the piece that enters the unit from the previous one.  As every piece
-        // has >= 16 tiles, no two pieces start in one block; blocks that no piece starts in lie
+        // has >= P tiles, no two pieces start in one block; blocks that no piece starts in lie
         // wholly inside one segment, which marks their slots empty -- so every slot the merge
         // reads is written exactly once.
 #pragma unroll
@@ -864,7 +869,7 @@ decode_split_kernel(DecodeArgs a) {
         alive = named_sync_and(bar_id, 128, ok && alive);
         {
             const int seg_j1 = seg_j0 + n_t;
-            const int own = cont ? a.splits : seg_j0 / kTilesPerSplit;
+            const int own = cont ? a.splits : seg_j0 / a.piece;
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 float* dst = slot_ptr(a, cb, hq0 + h, own);
@@ -874,9 +879,9 @@ decode_split_kernel(DecodeArgs a) {
                     dst[1] = lpart[h] + lpart[8 + h] + lpart[16 + h] + lpart[24 + h];
                 }
             }
-            const int n_blk = (c_nt + kTilesPerSplit - 1) / kTilesPerSplit;
+            const int n_blk = (c_nt + a.piece - 1) / a.piece;
             for (int k = r; k < n_blk; k += 128) {
-                const int k0 = k * kTilesPerSplit, k1 = min(k0 + kTilesPerSplit, c_nt);
+                const int k0 = k * a.piece, k1 = min(k0 + a.piece, c_nt);
                 if (k != own && k0 >= seg_j0 && k1 <= seg_j1) {
 #pragma unroll
                     for (int h = 0; h < GH; ++h) {
@@ -931,7 +936,7 @@ __global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
     const int n_sink = max(0, min(a.sink_len, a.seq_lens[b]));
     const float* base = slot_ptr(a, b, hq, 0);
     // the slots this (sequence, head) has: one per 16-tile block and the unit-entry slot
-    const int n_slots = nt > 0 ? (nt + kTilesPerSplit - 1) / kTilesPerSplit + 1 : 0;
+    const int n_slots = nt > 0 ? (nt + a.piece - 1) / a.piece + 1 : 0;
     auto slot_of = [&](int i) { return i + 1 == n_slots ? a.splits : i; };
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel's partials are visible
 
@@ -1033,12 +1038,12 @@ cudaError_t launch_dependent(Kern kern, dim3 grid, dim3 block, size_t smem, cuda
 
 // Persistent grid: two CTAs per SM, or fewer when at most max_stream_tiles full tiles (an upper
 // bound the host knows: sequences x units x block-table width) cannot keep them all busy with pieces
-// of >= kMinPiece tiles.
-int split_grid(long long max_stream_tiles) {
+// of >= piece tiles.
+int split_grid(long long max_stream_tiles, int piece) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    const long long pieces = (max_stream_tiles + kMinPiece - 1) / kMinPiece;
+    const long long pieces = (max_stream_tiles + piece - 1) / piece;
     const long long ctas = (pieces + kWorkers - 1) / kWorkers;
     return (int)(ctas < 1 ? 1 : (ctas < 2 * sms ? ctas : 2 * sms));
 }
@@ -1063,10 +1068,12 @@ cudaError_t run_split_g(const DecodeArgs& a, int gh, int grid, cudaStream_t stre
 }  // namespace
 
 // Workspace: the partial slots [B][Hq][splits + 1][132] f32, rounded up to 256 bytes.
-DecodePlan plan_decode(int B, int Hq, int /*Hkv*/, int max_tiles) {
+DecodePlan plan_decode(int B, int Hq, int Hkv, int max_tiles) {
     DecodePlan p;
-    p.tiles_per_split = kTilesPerSplit;
-    p.splits = max_tiles <= 0 ? 1 : (max_tiles + kTilesPerSplit - 1) / kTilesPerSplit;
+    const long long bound = (long long)B * Hkv * (max_tiles > 0 ? max_tiles : 0);  // full tiles at most
+    p.piece = kMaxPiece;
+    while (p.piece > kMinPieceTiles && bound < kFillWorkers * p.piece) p.piece /= 2;
+    p.splits = max_tiles <= 0 ? 1 : (max_tiles + p.piece - 1) / p.piece;
     p.workspace_bytes = ((size_t)B * Hq * (p.splits + 1) * kWsStride * sizeof(float) + 255) & ~(size_t)255;
     return p;
 }
@@ -1110,13 +1117,14 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.rotate = rotate;
     a.full_tail = full_tail;
     a.splits = plan.splits;
+    a.piece = plan.piece;
     a.B = B;
     const int gh = group;  // up to 8 heads x (hi, lo) fill the 16 MMA columns
     a.hblocks = group / gh;
     a.units = Hkv * a.hblocks;
     a.ws = static_cast<float*>(workspace);
     a.out = out;
-    const int grid = split_grid((long long)B * a.units * (max_tiles > 0 ? max_tiles : 0));
+    const int grid = split_grid((long long)B * a.units * (max_tiles > 0 ? max_tiles : 0), plan.piece);
     if (grid <= 0) return cudaErrorInvalidDevice;
     cudaError_t e;
     if (k_bits == 2 && v_bits == 2) e = run_split_g<2, 2>(a, gh, grid, stream);

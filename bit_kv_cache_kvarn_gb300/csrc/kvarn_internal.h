@@ -27,9 +27,10 @@ cudaError_t launch_dequant(int bits, int kind, const void* codes, const void* pa
                            const float* tile_scale, int64_t n_tiles, int original_basis,
                            int rotate, float* out, cudaStream_t stream);
 
-// Split-K layout for decode attention: partial-slot granularity, slot count and workspace size.
+// Split-K layout for decode attention: piece granularity P (minimum piece and tiles per partial
+// slot block), slot count and workspace size.
 struct DecodePlan {
-    int tiles_per_split;
+    int piece;
     int splits;
     size_t workspace_bytes;
 };

@@ -167,16 +167,22 @@ def test_workspace_plan(lib):
 
     cfg = _cfg()
 
-    def expected(B, Hq, max_tiles):
-        # partial slots: one per 16-tile block plus one; (m, l, 2 pad, o[128]) floats per slot,
-        # rounded up to 256 bytes
+    def expected(B, Hq, Hkv, max_tiles):
+        # piece granularity P: 16, halved (down to 2) while B Hkv max_tiles < 512 P; partial slots:
+        # one per P-tile block plus one; (m, l, 2 pad, o[128]) floats per slot, rounded up to 256 bytes
+        p = 16
+        while p > 2 and B * Hkv * max_tiles < 512 * p:
+            p //= 2
         up = lambda x: (x + 255) // 256 * 256
-        slots = max(1, -(-max_tiles // 16)) + 1
+        slots = max(1, -(-max_tiles // p)) + 1
         return up(B * Hq * slots * 132 * 4)
 
-    assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == expected(16, 32, 256)
-    assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == expected(4, 40, 1024)
-    assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == expected(1, 4, 0)
+    assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == expected(16, 32, 8, 256)
+    assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == expected(4, 40, 10, 1024)
+    assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == expected(1, 4, 1, 0)
+    # small calls take finer pieces: B = 1, 8 kv heads, 32 tiles -> P = 2, 17 slots per head
+    assert kv.kvarn_decode_workspace_size(cfg, 1, 32, 8, 32) == expected(1, 32, 8, 32) == 32 * 17 * 528
+    assert expected(2, 32, 8, 256) == 2 * 32 * (256 // 8 + 1) * 528  # 4096 tiles: P = 8
     assert kv.kvarn_decode_workspace_size(cfg, 1, 6, 4, 1) == 0
 
 
