@@ -102,6 +102,24 @@ def test_small_shapes_lengths_and_tails(kv, preset):
     assert torch.all(gpu[0] == 0)
 
 
+@pytest.mark.parametrize("B,hkv,lens_tiles,piece", [
+    (5, 4, [0, 3, 37, 150, 64], 4),          # stream bound 5 x 4 x 151 = 3020 tiles: P = 4
+    (6, 4, [1, 250, 17, 128, 99, 200], 8),   # 6 x 4 x 251 = 6024 tiles: P = 8
+])
+def test_piece_granularities_with_ragged_lengths(kv, B, hkv, lens_tiles, piece):
+    # the split kernel's pieces and partial slots follow the granularity P the library picks from
+    # the shape; the other tests meet P = 2 (small) and P = 16 (full size)
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    lens = [t * 128 + (37 * i) % 128 for i, t in enumerate(lens_tiles)]
+    c = build_cache(kv, cfg, B, hkv, lens, seed=31 + piece)
+    hq = 2 * hkv
+    slots = -(-c["nt"] // piece) + 1
+    assert kv.kvarn_decode_workspace_size(cfg, B, hq, hkv, c["nt"]) == -(-(B * hq * slots * 528) // 256) * 256
+    q = kv.synthetic.queries(31, B, hq, device="cuda")
+    gpu = run_gpu(kv, cfg, q, hkv, c, 0.09)
+    print(f"P = {piece} worst rel-L2", check(gpu, oracle_out(cfg, q, hkv, c, 0.09)))
+
+
 @pytest.mark.parametrize("k_bits,v_bits,hq,hkv", [(2, 2, 3, 3), (4, 4, 4, 2), (2, 4, 16, 2), (4, 2, 8, 1)])
 def test_group_sizes_and_bit_widths(kv, k_bits, v_bits, hq, hkv):
     cfg = kv.make_config(k_bits, v_bits, 8, 0)
