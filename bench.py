@@ -255,9 +255,10 @@ def run_diagnostics():
 
 
 def run_latency():
-    """Decode latency of single calls at serving-like shapes (32q/8kv heads, 2-bit K and V, full
-    tiles, no tail): back-to-back calls timed with CUDA events, cache re-read from L2 where it fits
-    (not flushed), so the numbers show the call's own latency, not HBM time."""
+    """Decode latency of single calls at serving-like shapes (32q/8kv heads, 2-bit K and V; lengths
+    a multiple of 128, or with a 127-token bf16 tail): back-to-back calls timed with CUDA events,
+    cache re-read from L2 where it fits (not flushed), so the numbers show the call's own latency,
+    not HBM time."""
     import torch
 
     import bit_kv_cache_kvarn_gb300 as kv
@@ -266,8 +267,8 @@ def run_latency():
     cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
     dev = torch.device("cuda", 0)
     res = {}
-    for B, ctx in ((1, 4096), (1, 32768), (4, 8192), (16, 32768)):
-        nt = ctx // 128
+    for B, ctx in ((1, 4096), (1, 32768), (4, 8192), (16, 32768), (1, 4096 + 127), (16, 32768 + 127)):
+        nt = -(-ctx // 128)  # block-table width; the last ctx % 128 tokens are the bf16 tail
         n = B * DEC_HKV * nt
         pool = min(n, 4096)  # distinct tiles; the block table cycles through them
         g = torch.Generator(device="cpu").manual_seed(11)
@@ -278,7 +279,7 @@ def run_latency():
         kv.kvarn_encode_kv_blocks(cfg, x, x, *pk, *pv)
         table = (torch.arange(n, dtype=torch.int32, device=dev) % pool).reshape(B, DEC_HKV, nt)
         lens = torch.full((B,), ctx, dtype=torch.int32, device=dev)
-        tail = torch.zeros(B, DEC_HKV, 128, 128, dtype=torch.bfloat16, device=dev)
+        tail = (torch.randn(B, DEC_HKV, 128, 128, generator=g) * 0.5).to(torch.bfloat16).to(dev)
         q = torch.randn(B, DEC_HQ, 128, generator=g).to(torch.bfloat16).to(dev)
         ws = torch.empty(kv.kvarn_decode_workspace_size(cfg, B, DEC_HQ, DEC_HKV, nt), dtype=torch.uint8, device=dev)
         out = torch.empty(B, DEC_HQ, 128, device=dev)

@@ -925,86 +925,181 @@ decode_split_kernel(DecodeArgs a) {
     if (warp == 0) tc::dealloc(tmem, kTmemCols);
 }
 
-// One warp per (sequence, query head): merge splits, inverse rotation, bf16 tail, normalise.
-__global__ void __launch_bounds__(32) decode_merge_kernel(DecodeArgs a) {
-    const int lane = threadIdx.x;
+// Max and sum over the merge CTA's 128 threads (every thread gets the result); red holds 4 floats.
+__device__ __forceinline__ float merge_max(float v, float* red) {
+    v = warp_max(v);
+    __syncthreads();  // red is free again
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+}
+__device__ __forceinline__ float merge_sum(float v, float* red) {
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+// Unnormalised Sylvester Walsh-Hadamard transform of 128 values, value i held by thread i: butterflies
+// on index bits 0-4 by shuffles, bits 5-6 through shared memory (stage: 128 floats).
+__device__ __forceinline__ float fwht128_block(float x, float* stage) {
+    const int c = threadIdx.x;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, x, s);
+        x = (c & s) ? y - x : x + y;
+    }
+#pragma unroll
+    for (int s = 32; s < kTile; s <<= 1) {
+        __syncthreads();
+        stage[c] = x;
+        __syncthreads();
+        const float y = stage[c ^ s];
+        x = (c & s) ? y - x : x + y;
+    }
+    return x;
+}
+
+// The 4 warps' float4 partials (channels 4 lane .. 4 lane + 3) summed for channel threadIdx.x.
+__device__ __forceinline__ float merge_warp_parts(float4 acc, float (*part)[kTile]) {
+    const int c = threadIdx.x;
+    __syncthreads();  // part is free again
+    *reinterpret_cast<float4*>(&part[c >> 5][4 * (c & 31)]) = acc;
+    __syncthreads();
+    return (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+}
+
+// One CTA of 128 threads per (sequence, query head), thread c owning output channel c:
+//   1. log-sum-exp merge of the partial slots (slot weights one per thread; the weighted o sums
+//      spread over the 4 warps, each lane reading 4 channels of a slot), then the inverse rotation;
+//   2. the unquantised tokens -- the FP16 sink, then the bf16 tail, in the original basis -- 128 at
+//      a time: thread t scores token t (its whole row at once), one online-softmax update per chunk,
+//      and the p-weighted V rows again spread over the warps;
+//   3. normalise by l.
+// Every load of a phase is independent of the others, so a chunk costs a few memory round trips
+// rather than one per token.
+__global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
+    __shared__ __align__(16) float s_q[kTile];     // scaled query, original basis
+    __shared__ __align__(16) float s_w[kTile];     // slot weights / token probabilities of a chunk
+    __shared__ __align__(16) float s_part[4][kTile];
+    __shared__ float s_red[4];
+    const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
     const int hq = blockIdx.x, b = blockIdx.y;
+    // programmatic dependent launch: the split grid (and everything before it) is complete and
+    // visible once this returns; nothing is read before it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int kvh = hq / a.group;
     const int len = body_len(a, b);
     const int nt = n_full_tiles(len, a.full_tail);
     const int tail = len - nt * kTile;  // 0..127, or 1..128 with the full window
     const int n_sink = max(0, min(a.sink_len, a.seq_lens[b]));
     const float* base = slot_ptr(a, b, hq, 0);
-    // the slots this (sequence, head) has: one per 16-tile block and the unit-entry slot
+    // the slots this (sequence, head) has: one per P-tile block and the unit-entry slot
     const int n_slots = nt > 0 ? (nt + a.piece - 1) / a.piece + 1 : 0;
     auto slot_of = [&](int i) { return i + 1 == n_slots ? a.splits : i; };
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel's partials are visible
 
-    float mmax = -INFINITY;
-    for (int i = lane; i < n_slots; i += 32) mmax = fmaxf(mmax, base[slot_of(i) * kWsStride]);
-    mmax = warp_max(mmax);
-    float l = 0.f;
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mmax != -INFINITY) {
-        // 32 slots at a time: each lane weighs one slot, then every lane adds the weighted o of
-        // each slot for its 4 channels (the loads of a chunk are independent of one another)
-        for (int c0 = 0; c0 < n_slots; c0 += 32) {
-            const int i = c0 + lane;
-            float f = 0.f;
+    float mloc = -INFINITY;
+    for (int i = c; i < n_slots; i += kTile) mloc = fmaxf(mloc, __ldcg(base + slot_of(i) * kWsStride));
+    float mmax = merge_max(mloc, s_red);
+    float l = 0.f, o = 0.f;
+    if (mmax != -INFINITY) {  // uniform over the CTA
+        float lloc = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k0 = 0; k0 < n_slots; k0 += kTile) {
+            const int i = k0 + c;
+            float w = 0.f;
             if (i < n_slots) {
-                const float m = base[slot_of(i) * kWsStride];
+                const float m = __ldcg(base + slot_of(i) * kWsStride);
                 if (m != -INFINITY) {  // an empty slot (its o is not written) weighs 0
-                    f = exp2f(m - mmax);
-                    l = fmaf(base[slot_of(i) * kWsStride + 1], f, l);
+                    w = exp2f(m - mmax);
+                    lloc = fmaf(__ldcg(base + slot_of(i) * kWsStride + 1), w, lloc);
                 }
             }
-            const int n_c = min(32, n_slots - c0);
+            __syncthreads();  // s_w is free again
+            s_w[c] = w;
+            __syncthreads();
+            const int n_c = min(kTile, n_slots - k0);
 #pragma unroll 4
-            for (int j = 0; j < n_c; ++j) {
-                const float fj = __shfl_sync(0xffffffffu, f, j);
-                if (fj == 0.f) continue;
-                const float4 v = *reinterpret_cast<const float4*>(base + slot_of(c0 + j) * kWsStride + 4 + 4 * lane);
-                o[0] = fmaf(v.x, fj, o[0]);
-                o[1] = fmaf(v.y, fj, o[1]);
-                o[2] = fmaf(v.z, fj, o[2]);
-                o[3] = fmaf(v.w, fj, o[3]);
+            for (int j = warp; j < n_c; j += 4) {
+                const float wj = s_w[j];
+                if (wj == 0.f) continue;
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(base + slot_of(k0 + j) * kWsStride + 4) + lane);
+                acc.x = fmaf(v.x, wj, acc.x);
+                acc.y = fmaf(v.y, wj, acc.y);
+                acc.z = fmaf(v.z, wj, acc.z);
+                acc.w = fmaf(v.w, wj, acc.w);
             }
         }
-        l = warp_sum(l);
-        if (a.rotate) {
-            fwht128_warp(o, lane);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) o[m] *= kInvSqrt128;
-        }
+        l = merge_sum(lloc, s_red);
+        o = merge_warp_parts(acc, s_part);
+        if (a.rotate) o = fwht128_block(o, s_w) * kInvSqrt128;
     }
-    if (tail > 0 || n_sink > 0) {
-        // the unquantised tokens: the FP16 sink, then the tail, in the original basis
-        const __nv_bfloat16* qp = a.q + ((size_t)b * a.Hq + hq) * kTile + 4 * lane;
-        float qv[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) qv[m] = __bfloat162float(qp[m]) * a.qscale;
+
+    const int n_tok = n_sink + tail;
+    if (n_tok > 0) {
+        s_q[c] = __bfloat162float(a.q[((size_t)b * a.Hq + hq) * kTile + c]) * a.qscale;
         const size_t tb = ((size_t)b * a.Hkv + kvh) * kTile * kTile;
-        for (int t = 0; t < n_sink + tail; ++t) {
-            const bool in_sink = t < n_sink;
-            const size_t row = tb + (size_t)(in_sink ? t : t - n_sink) * kTile + 4 * lane;
-            const __nv_bfloat16* kt = (in_sink ? a.k_sink : a.k_tail) + row;
-            const __nv_bfloat16* vt = (in_sink ? a.v_sink : a.v_tail) + row;
-            float d = 0.f;
+        __syncthreads();
+        for (int t0 = 0; t0 < n_tok; t0 += kTile) {
+            const int t = t0 + c;
+            float sc = -INFINITY;
+            if (t < n_tok) {
+                const bool in_sink = t < n_sink;
+                const uint4* kr = reinterpret_cast<const uint4*>((in_sink ? a.k_sink : a.k_tail) + tb +
+                                                                 (size_t)(in_sink ? t : t - n_sink) * kTile);
+                uint4 raw[16];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) d = fmaf(qv[m], __bfloat162float(kt[m]), d);
-            d = warp_sum(d);
-            const float m_new = fmaxf(mmax, d);
-            const float al = exp2f(mmax - m_new);
-            const float p = exp2f(d - m_new);
-            l = fmaf(l, al, p);
+                for (int i = 0; i < 16; ++i) raw[i] = __ldg(kr + i);
+                float d = 0.f;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) o[m] = fmaf(o[m], al, p * __bfloat162float(vt[m]));
+                for (int i = 0; i < 16; ++i) {
+                    const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+                    const float4 q0 = *reinterpret_cast<const float4*>(&s_q[8 * i]);
+                    const float4 q1 = *reinterpret_cast<const float4*>(&s_q[8 * i + 4]);
+                    const float2 k0 = __bfloat1622float2(kp[0]), k1 = __bfloat1622float2(kp[1]);
+                    const float2 k2 = __bfloat1622float2(kp[2]), k3 = __bfloat1622float2(kp[3]);
+                    d = fmaf(q0.x, k0.x, d);
+                    d = fmaf(q0.y, k0.y, d);
+                    d = fmaf(q0.z, k1.x, d);
+                    d = fmaf(q0.w, k1.y, d);
+                    d = fmaf(q1.x, k2.x, d);
+                    d = fmaf(q1.y, k2.y, d);
+                    d = fmaf(q1.z, k3.x, d);
+                    d = fmaf(q1.w, k3.y, d);
+                }
+                sc = d;
+            }
+            const float m_new = fmaxf(mmax, merge_max(sc, s_red));
+            const float al = exp2f(mmax - m_new);  // 0 while nothing came before
+            const float p = t < n_tok ? exp2f(sc - m_new) : 0.f;
+            l = fmaf(l, al, merge_sum(p, s_red));
+            __syncthreads();  // s_w is free again
+            s_w[c] = p;
+            __syncthreads();
+            const int n_c = min(kTile, n_tok - t0);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int j = warp; j < n_c; j += 4) {
+                const int tt = t0 + j;
+                const bool in_sink = tt < n_sink;
+                const __nv_bfloat16* vr = (in_sink ? a.v_sink : a.v_tail) + tb +
+                                          (size_t)(in_sink ? tt : tt - n_sink) * kTile + 4 * lane;
+                const uint2 raw = __ldg(reinterpret_cast<const uint2*>(vr));
+                const float2 v0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+                const float2 v1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+                const float pj = s_w[j];
+                acc.x = fmaf(pj, v0.x, acc.x);
+                acc.y = fmaf(pj, v0.y, acc.y);
+                acc.z = fmaf(pj, v1.x, acc.z);
+                acc.w = fmaf(pj, v1.y, acc.w);
+            }
+            o = fmaf(o, al, merge_warp_parts(acc, s_part));
             mmax = m_new;
         }
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    float4 r = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-    *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + hq) * kTile + 4 * lane) = r;
+    a.out[((size_t)b * a.Hq + hq) * kTile + c] = o * inv;
 }
 
 template <int KB, int VB, int GH>
@@ -1132,7 +1227,7 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     else if (k_bits == 2 && v_bits == 4) e = run_split_g<2, 4>(a, gh, grid, stream);
     else e = run_split_g<4, 4>(a, gh, grid, stream);
     if (e != cudaSuccess) return e;
-    return launch_dependent(decode_merge_kernel, dim3(Hq, B), dim3(32), 0, stream, a);
+    return launch_dependent(decode_merge_kernel, dim3(Hq, B), dim3(kTile), 0, stream, a);
 }
 
 }  // namespace kvarn
