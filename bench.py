@@ -254,6 +254,31 @@ def run_diagnostics():
                       "presets": res}), flush=True)
 
 
+def graph_us(fn, reps):
+    """Per-call device time of fn (one library call) replayed from a CUDA graph: the host enqueues
+    nothing per call, so the number excludes the binding's and the launches' host overhead."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()  # warm-up outside the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    c.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(c) / reps * 1000
+
+
 def run_latency():
     """Decode latency of single calls at serving-like shapes (32q/8kv heads, 2-bit K and V; lengths
     a multiple of 128, or with a 127-token bf16 tail): back-to-back calls timed with CUDA events,
@@ -298,10 +323,13 @@ def run_latency():
             call()
         c.record()
         torch.cuda.synchronize()
-        res[f"B={B}, ctx={ctx}"] = round(a.elapsed_time(c) / reps * 1000, 2)
+        res[f"B={B}, ctx={ctx}"] = {"eager_us": round(a.elapsed_time(c) / reps * 1000, 2),
+                                    "graph_us": round(graph_us(call, reps), 2)}
     assert kv.kvarn_device_error() == 0
-    print(json.dumps({"impl": "latency", "unit": "us per call", "heads": f"{DEC_HQ}q/{DEC_HKV}kv",
-                      "preset": "kvarn_k2v2_g128", "results": res}), flush=True)
+    print(json.dumps({"impl": "latency", "unit": "us per call",
+                      "eager": "back-to-back calls from Python (host enqueue cost included when it exceeds the device time)",
+                      "graph": "the same call replayed from a CUDA graph (device time)",
+                      "heads": f"{DEC_HQ}q/{DEC_HKV}kv", "preset": "kvarn_k2v2_g128", "results": res}), flush=True)
 
 
 def run_append_timing():
@@ -341,9 +369,14 @@ def run_append_timing():
             torch.cuda.synchronize()
             times.append(a.elapsed_time(c) * 1000)
         assert kv.kvarn_device_error() == 0
+        lens.zero_()
+        reps = 128 if n_new == 1 else 32  # stays inside the block table without a host-side reset
+        g_us = graph_us(lambda: kv.kvarn_append_tokens(cfg, kn, kn, lens, kt, vt, *pools, table, ws), reps)
+        assert kv.kvarn_device_error() == 0
         res[f"n_new={n_new}"] = {"mean_us": round(statistics.mean(times), 2),
                                  "median_us": round(statistics.median(times), 2),
-                                 "max_us": round(max(times), 2), "steps": steps}
+                                 "max_us": round(max(times), 2), "steps": steps,
+                                 "graph_us": round(g_us, 2)}
     print(json.dumps({"impl": "append", "shape": f"B={B}, Hkv={H}, k2v2", "results": res}), flush=True)
 
 

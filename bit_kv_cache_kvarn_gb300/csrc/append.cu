@@ -7,9 +7,10 @@
 // speculative step's rejected tokens never reach the cache.
 //
 // One block of threads per sequence moves the tokens of every kv head (16-byte copies) and, when
-// the sequence's block completes, copies it to a compact staging area and records the pool slot
-// it belongs to; the encoder then runs over the staged tiles only (device-side count) and writes
-// each to its slot.
+// the sequence's block completes, copies it to the staging slot of its (sequence, kv head) and
+// records the pool tile it belongs to (-1 for slots with nothing staged); one encoder launch over K
+// and V then encodes the staged slots into their pool tiles and skips the others.  Two launches per
+// call, whatever number of blocks completes.
 #include "kvarn_common.cuh"
 #include "kvarn_internal.h"
 
@@ -32,7 +33,6 @@ __device__ __forceinline__ void copy_rows(__nv_bfloat16* dst, const __nv_bfloat1
 
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     const int b = blockIdx.x;
-    __shared__ int s_slot;
     const int len = a.seq_lens[b];
     int acc = a.n_accept != nullptr ? a.n_accept[b] : a.n_new;
     acc = acc < 0 ? 0 : (acc > a.n_new ? a.n_new : acc);
@@ -50,11 +50,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     }
     if (complete && (blk >= a.max_tiles || len < 0)) {
         if (threadIdx.x == 0) atomicOr(&g_append_error, 1u);
+        for (int h = threadIdx.x; h < a.Hkv; h += kThreads) a.dest[(size_t)b * a.Hkv + h] = -1;
         return;
     }
     const int need = complete ? kTile - t0 : acc;  // new tokens that go into the current block
-    if (complete && threadIdx.x == 0) s_slot = atomicAdd(a.count, a.Hkv);
-    __syncthreads();
+    if (!complete)
+        for (int h = threadIdx.x; h < a.Hkv; h += kThreads) a.dest[(size_t)b * a.Hkv + h] = -1;
     for (int h = 0; h < a.Hkv; ++h) {
         const size_t u = (size_t)b * a.Hkv + h;
         __nv_bfloat16* kt = a.k_tail + u * kTile * kTile;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         const __nv_bfloat16* kn = a.k_new + u * a.n_new * kTile;
         const __nv_bfloat16* vn = a.v_new + u * a.n_new * kTile;
         if (complete) {
-            const int slot = s_slot + h;
+            const size_t slot = u;
             __nv_bfloat16* ks = a.k_stage + (size_t)slot * kTile * kTile;
             __nv_bfloat16* vs = a.v_stage + (size_t)slot * kTile * kTile;
             copy_rows(ks, kt, t0);
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
 
 size_t append_workspace_bytes(int B, int Hkv) {
     const size_t tiles = (size_t)B * Hkv;
-    return 2 * tiles * kTile * kTile * sizeof(__nv_bfloat16) + ((tiles * sizeof(int32_t) + 255) & ~(size_t)255) + 256;
+    return 2 * tiles * kTile * kTile * sizeof(__nv_bfloat16) + ((tiles * sizeof(int32_t) + 255) & ~(size_t)255);
 }
 
 cudaError_t read_and_clear_append_error(unsigned int* out) {
@@ -100,18 +101,13 @@ cudaError_t read_and_clear_append_error(unsigned int* out) {
 cudaError_t launch_append(const AppendArgs& a, int B, int k_bits, int v_bits, int iters, int rotate,
                           int normalize, void* k_codes, void* k_params, float* k_scale, void* v_codes,
                           void* v_params, float* v_scale, cudaStream_t stream) {
-    cudaError_t e = cudaMemsetAsync(a.count, 0, sizeof(int32_t), stream);
-    if (e != cudaSuccess) return e;
     append_kernel<<<B, kThreads, 0, stream>>>(a);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // encode the staged blocks (a device-side count, at most B * Hkv) into their pool slots
-    const int64_t max_tiles = (int64_t)B * a.Hkv;
-    e = launch_encode(k_bits, KVARN_KIND_K, a.k_stage, max_tiles, k_codes, k_params, k_scale, iters, rotate,
-                      normalize, stream, a.count, a.dest);
-    if (e != cudaSuccess) return e;
-    return launch_encode(v_bits, KVARN_KIND_V, a.v_stage, max_tiles, v_codes, v_params, v_scale, iters, rotate,
-                         normalize, stream, a.count, a.dest);
+    // encode the staged blocks (dest >= 0) of every (sequence, kv head) slot into their pool tiles
+    const int64_t slots = (int64_t)B * a.Hkv;
+    return launch_encode_kv(k_bits, v_bits, a.k_stage, slots, k_codes, k_params, k_scale, a.v_stage, slots,
+                            v_codes, v_params, v_scale, iters, rotate, normalize, stream, a.dest);
 }
 
 }  // namespace kvarn

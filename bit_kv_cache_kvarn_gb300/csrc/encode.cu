@@ -511,28 +511,27 @@ __device__ __forceinline__ bool encode_wait(EncodeSmem& sm, int local) {
     return false;
 }
 
-// Tiles of one kind.  Optional device-side tile count n_dev (at most n_tiles) and output slots
-// (dest[i] for input tile i).
+// Tiles of one kind.
 template <int BITS, int KIND>
 __global__ void __launch_bounds__(kThreads, 2)
 encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ codes_out,
               uint8_t* __restrict__ params_out, float* __restrict__ scale_out, int iters,
-              int rotate, int normalize, const int32_t* __restrict__ n_dev,
-              const int32_t* __restrict__ dest) {
+              int rotate, int normalize) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
-    if (n_dev != nullptr) n_tiles = min(n_tiles, (int64_t)max(*n_dev, 0));
     encode_prologue(sm, blockIdx.x < n_tiles ? x + (int64_t)blockIdx.x * kTile * kTile : nullptr);
     int local = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
         if (!encode_wait(sm, local)) break;
         const int64_t nt = tile + gridDim.x;
         encode_tile<BITS, KIND>(sm, nt < n_tiles ? x + nt * kTile * kTile : nullptr, codes_out, params_out,
-                                scale_out, dest != nullptr ? (int64_t)dest[tile] : tile, iters, rotate, normalize);
+                                scale_out, tile, iters, rotate, normalize);
     }
 }
 
 // The K and V tiles of one call in one grid: virtual tile i < n_k is K tile i, else V tile i - n_k.
+// With dest, input tile u (of either kind) goes to output slot dest[u] and is skipped when dest[u]
+// is negative (the append path stages one slot per (sequence, kv head), most of them unused).
 struct EncodeKV {
     const __nv_bfloat16* kx;
     const __nv_bfloat16* vx;
@@ -543,6 +542,7 @@ struct EncodeKV {
     uint8_t* v_codes;
     uint8_t* v_params;
     float* v_scale;
+    const int32_t* dest;  // [n_k] output slots shared by K and V (n_k == n_v), or null
     int iters, rotate, normalize;
 };
 
@@ -550,23 +550,34 @@ __device__ __forceinline__ const __nv_bfloat16* kv_src(const EncodeKV& a, int64_
     return i < a.n_k ? a.kx + i * kTile * kTile : a.vx + (i - a.n_k) * kTile * kTile;
 }
 
+// The first virtual tile at or after i, stepping by the grid, that is to be encoded (n if none).
+__device__ __forceinline__ int64_t kv_next(const EncodeKV& a, int64_t i, int64_t n) {
+    if (a.dest == nullptr) return i < n ? i : n;
+    for (; i < n; i += gridDim.x)
+        if (a.dest[i < a.n_k ? i : i - a.n_k] >= 0) return i;
+    return n;
+}
+
 template <int KB, int VB>
 __global__ void __launch_bounds__(kThreads, 2) encode_kv_kernel(EncodeKV a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const int64_t n = a.n_k + a.n_v;
-    encode_prologue(sm, blockIdx.x < n ? kv_src(a, blockIdx.x) : nullptr);
-    int local = 0;
-    for (int64_t tile = blockIdx.x; tile < n; tile += gridDim.x, ++local) {
+    int64_t tile = kv_next(a, blockIdx.x, n);
+    encode_prologue(sm, tile < n ? kv_src(a, tile) : nullptr);
+    for (int local = 0; tile < n; ++local) {
         if (!encode_wait(sm, local)) break;
-        const int64_t nt = tile + gridDim.x;
+        const int64_t nt = kv_next(a, tile + gridDim.x, n);
         const __nv_bfloat16* next = nt < n ? kv_src(a, nt) : nullptr;
+        const int64_t u = tile < a.n_k ? tile : tile - a.n_k;
+        const int64_t slot = a.dest != nullptr ? (int64_t)a.dest[u] : u;
         if (tile < a.n_k)
-            encode_tile<KB, KVARN_KIND_K>(sm, next, a.k_codes, a.k_params, a.k_scale, tile, a.iters, a.rotate,
+            encode_tile<KB, KVARN_KIND_K>(sm, next, a.k_codes, a.k_params, a.k_scale, slot, a.iters, a.rotate,
                                           a.normalize);
         else
-            encode_tile<VB, KVARN_KIND_V>(sm, next, a.v_codes, a.v_params, a.v_scale, tile - a.n_k, a.iters,
+            encode_tile<VB, KVARN_KIND_V>(sm, next, a.v_codes, a.v_params, a.v_scale, slot, a.iters,
                                           a.rotate, a.normalize);
+        tile = nt;
     }
 }
 
@@ -585,7 +596,7 @@ cudaError_t read_and_clear_device_error(unsigned int* out) {
 
 cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
-                          cudaStream_t stream, const int32_t* n_dev, const int32_t* dest) {
+                          cudaStream_t stream) {
     int dev = 0, sms = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -601,7 +612,7 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
         kern<<<grid, kThreads, smem, stream>>>(static_cast<const __nv_bfloat16*>(x), n_tiles,
                                                static_cast<uint8_t*>(codes),
                                                static_cast<uint8_t*>(params), tile_scale, iters,
-                                               rotate, normalize, n_dev, dest);
+                                               rotate, normalize);
         return cudaGetLastError();
     };
     if (bits == 2 && kind == KVARN_KIND_K) return run(encode_kernel<2, KVARN_KIND_K>);
@@ -615,7 +626,7 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
 cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_k, void* k_codes,
                              void* k_params, float* k_scale, const void* v_x, int64_t n_v, void* v_codes,
                              void* v_params, float* v_scale, int iters, int rotate, int normalize,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const int32_t* dest) {
     if (n_k + n_v == 0) return cudaSuccess;
     int dev = 0, sms = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -636,6 +647,7 @@ cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_
     a.v_codes = static_cast<uint8_t*>(v_codes);
     a.v_params = static_cast<uint8_t*>(v_params);
     a.v_scale = v_scale;
+    a.dest = dest;
     a.iters = iters;
     a.rotate = rotate;
     a.normalize = normalize;

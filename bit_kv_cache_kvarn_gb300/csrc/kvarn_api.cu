@@ -339,8 +339,6 @@ kvarn_status kvarn_append_tokens(const kvarn_config* cfg, int B, int Hkv, const 
     a.k_stage = reinterpret_cast<__nv_bfloat16*>(w);
     a.v_stage = reinterpret_cast<__nv_bfloat16*>(w + tiles * KVARN_TILE_TOKENS * KVARN_TILE_TOKENS * 2);
     a.dest = reinterpret_cast<int32_t*>(w + 2 * tiles * KVARN_TILE_TOKENS * KVARN_TILE_TOKENS * 2);
-    a.count = reinterpret_cast<int32_t*>(w + 2 * tiles * KVARN_TILE_TOKENS * KVARN_TILE_TOKENS * 2 +
-                                         ((tiles * sizeof(int32_t) + 255) & ~(size_t)255));
     cudaError_t e = kvarn::launch_append(a, B, cfg->k_bits, cfg->v_bits, cfg->sinkhorn_iters,
                                          !(cfg->flags & KVARN_FLAG_NO_ROTATE),
                                          !(cfg->flags & KVARN_FLAG_NO_NORMALIZE), k_codes, k_params, k_scale,

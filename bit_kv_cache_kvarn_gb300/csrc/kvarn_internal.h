@@ -11,17 +11,16 @@ namespace kvarn {
 size_t encode_smem_bytes();
 cudaError_t read_and_clear_device_error(unsigned int* out);
 cudaError_t read_and_clear_decode_error(unsigned int* out);
-// n_dev (optional): device-side tile count, at most n_tiles; dest (optional): output slot of input
-// tile i.
 cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, void* codes,
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
-                          cudaStream_t stream, const int32_t* n_dev = nullptr,
-                          const int32_t* dest = nullptr);
+                          cudaStream_t stream);
 
+// K tiles then V tiles in one grid.  dest (optional, device, [n_k] with n_k == n_v): input tile u of
+// either kind goes to output slot dest[u], and is skipped when dest[u] < 0.
 cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_k, void* k_codes,
                              void* k_params, float* k_scale, const void* v_x, int64_t n_v, void* v_codes,
                              void* v_params, float* v_scale, int iters, int rotate, int normalize,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const int32_t* dest = nullptr);
 
 cudaError_t launch_dequant(int bits, int kind, const void* codes, const void* params,
                            const float* tile_scale, int64_t n_tiles, int original_basis,
@@ -54,10 +53,9 @@ struct AppendArgs {
     __nv_bfloat16* k_tail;       // [B][Hkv][128][128], updated
     __nv_bfloat16* v_tail;
     const int32_t* block_table;  // [B][Hkv][max_tiles]
-    __nv_bfloat16* k_stage;      // workspace: [B * Hkv][128][128] staged blocks
+    __nv_bfloat16* k_stage;      // workspace: [B * Hkv][128][128], slot b * Hkv + h
     __nv_bfloat16* v_stage;
-    int32_t* dest;               // workspace: [B * Hkv] pool slot of each staged tile
-    int32_t* count;              // workspace: number of staged tiles
+    int32_t* dest;               // workspace: [B * Hkv] pool tile of each staged block, -1 if none
 };
 size_t append_workspace_bytes(int B, int Hkv);
 cudaError_t launch_append(const AppendArgs& a, int B, int k_bits, int v_bits, int iters, int rotate,

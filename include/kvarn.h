@@ -234,8 +234,9 @@ kvarn_status kvarn_decode_attention_static_ws(
     const int32_t* seq_lens_host, const void* k_tail_bf16, const void* v_tail_bf16,
     float softmax_scale, float* out, kvarn_stream_t stream);
 
-/* Bytes of device workspace kvarn_append_tokens needs: staging for B*Hkv K and V blocks
- * (2 x 32 KiB each), their pool slots and a counter.  0 for an invalid shape. */
+/* Bytes of device workspace kvarn_append_tokens needs: one staging slot per (sequence, kv head)
+ * for a K and a V block (2 x 32 KiB each) and the slots' pool tiles (int32, rounded up to 256
+ * bytes).  0 for an invalid shape. */
 size_t kvarn_append_workspace_size(int B, int Hkv);
 
 /* Commit the first n_accept[b] of n_new offered tokens of each sequence to its cache
@@ -255,7 +256,7 @@ size_t kvarn_append_workspace_size(int B, int Hkv);
  *   workspace   : >= kvarn_append_workspace_size(B, Hkv) bytes, 256-byte aligned.
  * A sequence whose completed block has no entry in the block table (index >= max_tiles) is left
  * unchanged and bit 3 (value 4) of kvarn_device_error is set.  Host-side errors as elsewhere;
- * nothing is enqueued on error.  Launches: one append kernel and two encode kernels. */
+ * nothing is enqueued on error.  Launches: one append kernel and one encode kernel (K and V). */
 kvarn_status kvarn_append_tokens(const kvarn_config* cfg, int B, int Hkv, const void* k_new_bf16,
                                  const void* v_new_bf16, int n_new, const int32_t* n_accept,
                                  int32_t* seq_lens, void* k_tail_bf16, void* v_tail_bf16, void* k_codes,
