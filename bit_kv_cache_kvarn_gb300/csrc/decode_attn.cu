@@ -9,8 +9,8 @@
 //   V (groups = tokens):   o_j += g s2_j (sum_t p_t S1_t code_tj + sum_t p_t Z_t)
 //
 // Split kernel (5th-generation tensor cores).  The full tiles of all (sequence, kv head) units form
-// one stream that every CTA cuts, from the sequence lengths, into equal contiguous pieces of >= 16
-// tiles; a CTA holds two warpgroup "workers", each processing its piece persistently.  Per tile,
+// one stream that every CTA cuts, from the sequence lengths, into equal contiguous pieces of >= P
+// tiles (P = 16, smaller for small calls); a CTA holds two warpgroup "workers", each processing its piece persistently.  Per tile,
 // lane 0 of each of the worker's four warps brings one of the tile's four blocks (K codes, V codes,
 // K parameters, V parameters) into a shared-memory ring with a 1-D TMA bulk copy (mbarrier-tracked);
 // then thread r of the worker:
@@ -26,9 +26,9 @@
 // and whether or not they share an accumulator), while MMAs issued by different warps overlap.
 // So each of the worker's 4 warps issues 2 of the 8 K-steps into its own 16-column partial
 // accumulator and the partials are summed on readout; the zero-point sums stay on the CUDA cores.
-// Merge kernel: one warp per (sequence, query head) merges the partial slots by log-sum-exp, applies
-// the inverse rotation, attends to the unquantised bf16 tail and normalises.  Two launches per call,
-// both with programmatic dependent launch.
+// Merge kernel: one 128-thread CTA per (sequence, query head) merges the partial slots by
+// log-sum-exp, applies the inverse rotation, attends to the unquantised sink and tail tokens and
+// normalises.  Two launches per call, both with programmatic dependent launch.
 #include <math.h>
 
 #include "kvarn_common.cuh"
@@ -68,10 +68,9 @@ constexpr float kLoScale = 2048.f;
 
 // A worker's piece of the tile stream.  The stream lists, sequence by sequence and unit by unit
 // (unit = kv head x head block), the full tiles of each unit; a piece is a contiguous run of it.
-struct PlanEntry {
-    int b, u, j, pad;    // first tile: sequence, unit, tile within the unit
-    long long len;       // number of tiles
-    long long pad2;
+struct Piece {
+    int b, u, j;     // first tile: sequence, unit, tile within the unit
+    long long len;   // number of tiles
 };
 
 struct DecodeArgs {
@@ -412,7 +411,7 @@ __device__ __forceinline__ long long cta_sum(long long v, long long* scratch) {
 // (unit = kv head x head block) -- is cut into w_used equal contiguous runs of >= P tiles,
 // worker w taking run w (none when w >= w_used); this balances the grid to a tile whatever the
 // length mix.  Every CTA computes it from the lengths (two passes over the sequences).
-__device__ PlanEntry find_piece(const DecodeArgs& a, int wk, long long* scratch) {
+__device__ Piece find_piece(const DecodeArgs& a, int wk, long long* scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     long long own = 0;
     for (int b = tid; b < a.B; b += kThreads) own += full_tiles(a, b);
@@ -428,10 +427,9 @@ __device__ PlanEntry find_piece(const DecodeArgs& a, int wk, long long* scratch)
         const long long w = (long long)blockIdx.x * kWorkers + k;
         g0[k] = w < w_used ? total * w / w_used : -1;
     }
-    PlanEntry e;
-    e.b = e.u = e.j = e.pad = 0;
+    Piece e;
+    e.b = e.u = e.j = 0;
     e.len = 0;
-    e.pad2 = 0;
     const long long w = (long long)blockIdx.x * kWorkers + wk;
     if (w < w_used) e.len = total * (w + 1) / w_used - total * w / w_used;
     // the sequence holding tile g0 of the stream: exclusive prefix sums of the tiles per sequence
@@ -528,7 +526,7 @@ decode_split_kernel(DecodeArgs a) {
     tc::fence_after();
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernels' writes are visible
     __shared__ long long s_scratch[kThreads / 32];
-    const PlanEntry piece = find_piece(a, wk, s_scratch);
+    const Piece piece = find_piece(a, wk, s_scratch);
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const uint32_t a_col = tmem + 128 * wk, d_col = a_col + 64;  // D: 4 partials x 16 columns
@@ -665,7 +663,7 @@ decode_split_kernel(DecodeArgs a) {
         named_sync(bar_id, 128);
 
         float m_run[GH], l_part[GH], o[GH];
-        // the item's rotated query for channel r and its scale, kept in registers for small groups
+        // the unit's rotated query for channel r and its scale, kept in registers for small groups
         constexpr bool kQReg = GH <= 4;
         float qreg[kQReg ? GH : 1], ereg[kQReg ? GH : 1];
 #pragma unroll
@@ -749,7 +747,7 @@ decode_split_kernel(DecodeArgs a) {
             // ---- online softmax over the tile's 128 tokens (thread r = token r), log2 domain ----
             // Lazy maximum: p = 2^(s - m) with the running maximum m while no score of the tile
             // exceeds it by more than kLazy (p <= 2^kLazy keeps p S1 kWScale inside fp16); otherwise
-            // (always on an item's first tile) the tile maximum is taken exactly and the partial
+            // (always on a segment's first tile) the tile maximum is taken exactly and the partial
             // sums are rescaled.
             float sc[GH], p[GH], zks[GH];
             const float tok = gk * e4m3_value(sb[St::kKP + 128 + r]);

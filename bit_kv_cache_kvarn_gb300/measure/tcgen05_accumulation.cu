@@ -6,6 +6,9 @@
 // Probe: accumulation precision of tcgen05.mma kind::f16 (fp16 in, fp32 out), M=128, N=16, K=16.
 // A = 1.0 everywhere; column n of B: k = 0 -> 1.0, k = 1..15 -> 2^-(6+n).  Exact D[*, n] = 1 + 15 * 2^-(6+n).
 // A second run uses subnormal A (2^-24) with B scaled by 2^14 / 2^(6+n) alike, like the decode kernel.
+// A third run has no large product: subnormal A (2^-24) and all sixteen B entries of column n equal to
+// 2^-n, so every product is 2^-(24+n) and the exact sum 2^-(20+n): it tells whether small products
+// are lost below a fixed size or only next to a much larger product.
 #include <cstdio>
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -19,7 +22,8 @@ __global__ void probe(float* out, int* err, int sub) {
     for (int i = tid; i < 256; i += blockDim.x) {
         const int k = i >> 4, n = i & 15;
         float v = (k == 0) ? 1.f : ldexpf(1.f, -(6 + n));
-        if (sub) v *= 16384.f;  // A is 2^-24 below: keep products in the same range as the decode kernel
+        if (sub == 1) v *= 16384.f;  // A is 2^-24 below: keep products in the same range as the decode kernel
+        if (sub == 2) v = ldexpf(1.f, -n);
         const int off = ((k >> 3) * 256 + (n >> 3) * 128 + (k & 7) * 16) / 2 + (n & 7);
         b[off] = __float2half_rn(v);
     }
@@ -76,14 +80,16 @@ __global__ void probe(float* out, int* err, int sub) {
 int main() {
     float* out; int* err;
     cudaMallocManaged(&out, 64); cudaMallocManaged(&err, 4); *err = 0;
-    for (int sub = 0; sub < 2; ++sub) {
+    for (int sub = 0; sub < 3; ++sub) {
         probe<<<1, 128>>>(out, err, sub);
         cudaError_t e = cudaDeviceSynchronize();
         if (e != cudaSuccess) { printf("err %s\n", cudaGetErrorString(e)); return 1; }
-        printf("%s\n", sub ? "A = 2^-24 (subnormal), B x 2^14" : "A = 1.0");
+        printf("%s\n", sub == 2 ? "A = 2^-24 (subnormal), all B of column n = 2^-n" :
+                        (sub ? "A = 2^-24 (subnormal), B x 2^14" : "A = 1.0"));
         for (int n = 0; n < 16; ++n) {
             double ex = 1.0 + 15.0 * ldexp(1.0, -(6 + n));
-            if (sub) ex = ex * 16384.0 * ldexp(1.0, -24);
+            if (sub == 1) ex = ex * 16384.0 * ldexp(1.0, -24);
+            if (sub == 2) ex = 16.0 * ldexp(1.0, -(24 + n));
             // fp16 B for n >= 9 is subnormal (2^-15 and below) in the A = 1.0 run
             printf("  n=%2d small=2^-%2d  got %.10e  exact %.10e  rel err %.2e\n", n, 6 + n, out[n], ex, (out[n] - ex) / ex);
         }

@@ -120,6 +120,24 @@ def test_piece_granularities_with_ragged_lengths(kv, B, hkv, lens_tiles, piece):
     print(f"P = {piece} worst rel-L2", check(gpu, oracle_out(cfg, q, hkv, c, 0.09)))
 
 
+def test_many_sequences_and_many_slots(kv):
+    # more sequences than one scan chunk of the split kernel's piece search (256), and one long
+    # unit with more partial slots than one chunk of the merge (128 slots at P = 2)
+    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
+    g = np.random.default_rng(41)
+    lens = [int(v) for v in g.integers(0, 5 * 128, size=300)]
+    c = build_cache(kv, cfg, 300, 1, lens, seed=41)
+    q = kv.synthetic.queries(41, 300, 2, device="cuda")
+    gpu = run_gpu(kv, cfg, q, 1, c, 0.09)
+    print("300 sequences worst rel-L2", check(gpu, oracle_out(cfg, q, 1, c, 0.09)))
+    lens = [300 * 128 + 50]
+    c = build_cache(kv, cfg, 1, 1, lens, seed=42)
+    assert kv.kvarn_decode_workspace_size(cfg, 1, 2, 1, c["nt"]) == -(-(2 * (-(-c["nt"] // 2) + 1) * 528) // 256) * 256
+    q = kv.synthetic.queries(42, 1, 2, device="cuda")
+    gpu = run_gpu(kv, cfg, q, 1, c, 0.09)
+    print("151 slots worst rel-L2", check(gpu, oracle_out(cfg, q, 1, c, 0.09)))
+
+
 @pytest.mark.parametrize("k_bits,v_bits,hq,hkv", [(2, 2, 3, 3), (4, 4, 4, 2), (2, 4, 16, 2), (4, 2, 8, 1)])
 def test_group_sizes_and_bit_widths(kv, k_bits, v_bits, hq, hkv):
     cfg = kv.make_config(k_bits, v_bits, 8, 0)
