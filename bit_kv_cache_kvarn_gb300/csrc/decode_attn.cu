@@ -114,6 +114,14 @@ __device__ __forceinline__ int n_full_tiles(int len, int full_tail) {
     return full_tail ? (len > 0 ? (len - 1) >> 7 : 0) : len >> 7;
 }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error within 2 ulp; results below
+// 2^-126 flush to 0, i.e. weights 2^-126 under the running maximum).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Shared-memory ring stage: K codes | V codes | K params | V params, one bulk copy each.
 template <int KB, int VB>
 struct Stage {
@@ -762,7 +770,7 @@ decode_split_kernel(DecodeArgs a) {
                 else ei = einv[h];
                 sc[h] = fmaf(dot, ei, zk * (ei * (1.f / kTwo24))) * tok;
                 over = over || !(sc[h] <= m_run[h] + kLazy);
-                p[h] = exp2f(sc[h] - m_run[h]);
+                p[h] = fast_exp2(sc[h] - m_run[h]);
             }
             const float w = e4m3_value(sb[St::kVP + r]) * (kWScale * pre_v);
             const float zval = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kVP + 256)[r]);
@@ -810,11 +818,11 @@ decode_split_kernel(DecodeArgs a) {
                 for (int h = 0; h < GH; ++h) {
                     const float mt = fmaxf(fmaxf(mpart[h], mpart[8 + h]), fmaxf(mpart[16 + h], mpart[24 + h]));
                     const float m_new = fmaxf(m_run[h], mt);
-                    const float alpha = exp2f(m_run[h] - m_new);
+                    const float alpha = fast_exp2(m_run[h] - m_new);
                     m_run[h] = m_new;
                     l_part[h] *= alpha;
                     o[h] *= alpha;
-                    p[h] = exp2f(sc[h] - m_new);
+                    p[h] = fast_exp2(sc[h] - m_new);
                 }
                 build_bv();
                 fence_proxy_async();
@@ -1010,7 +1018,7 @@ __global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
             if (i < n_slots) {
                 const float m = __ldcg(base + slot_of(i) * kWsStride);
                 if (m != -INFINITY) {  // an empty slot (its o is not written) weighs 0
-                    w = exp2f(m - mmax);
+                    w = fast_exp2(m - mmax);
                     lloc = fmaf(__ldcg(base + slot_of(i) * kWsStride + 1), w, lloc);
                 }
             }
@@ -1069,8 +1077,8 @@ __global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
                 sc = d;
             }
             const float m_new = fmaxf(mmax, merge_max(sc, s_red));
-            const float al = exp2f(mmax - m_new);  // 0 while nothing came before
-            const float p = t < n_tok ? exp2f(sc - m_new) : 0.f;
+            const float al = fast_exp2(mmax - m_new);  // 0 while nothing came before
+            const float p = t < n_tok ? fast_exp2(sc - m_new) : 0.f;
             l = fmaf(l, al, merge_sum(p, s_red));
             __syncthreads();  // s_w is free again
             s_w[c] = p;
