@@ -1142,8 +1142,7 @@ cudaError_t launch_dependent(Kern kern, dim3 grid, dim3 block, size_t smem, cuda
 // of >= piece tiles.
 int split_grid(long long max_stream_tiles, int piece) {
     int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (current_device(&dev, &sms) != cudaSuccess) return -1;
     const long long pieces = (max_stream_tiles + piece - 1) / piece;
     const long long ctas = (pieces + kWorkers - 1) / kWorkers;
     return (int)(ctas < 1 ? 1 : (ctas < 2 * sms ? ctas : 2 * sms));
@@ -1153,7 +1152,10 @@ template <int KB, int VB, int GH>
 cudaError_t run_split(const DecodeArgs& a, int grid, cudaStream_t stream) {
     auto kern = decode_split_kernel<KB, VB, GH>;
     const size_t smem = split_smem_bytes<KB, VB, GH>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = set_smem_limit_once(kern, (int)smem, false, dev);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, stream, a);
 }

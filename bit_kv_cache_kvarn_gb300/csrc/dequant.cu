@@ -121,7 +121,10 @@ cudaError_t launch_dequant(int bits, int kind, const void* codes, const void* pa
     const size_t smem = (size_t)(kTile * kYStride + 3 * kTile) * sizeof(float);
     dim3 grid((unsigned)n_tiles);  // the API limits n_tiles to 2^31 - 1
     auto run = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = set_smem_limit_once(kern, (int)smem, false, dev);
         if (e != cudaSuccess) return e;
         kern<<<grid, kThreads, smem, stream>>>(c, p, tile_scale, out, original_basis, rotate);
         return cudaGetLastError();

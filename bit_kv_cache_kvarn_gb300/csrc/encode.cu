@@ -598,16 +598,12 @@ cudaError_t launch_encode(int bits, int kind, const void* x, int64_t n_tiles, vo
                           void* params, float* tile_scale, int iters, int rotate, int normalize,
                           cudaStream_t stream) {
     int dev = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t err = current_device(&dev, &sms);
     if (err != cudaSuccess) return err;
     const int grid = (int)(n_tiles < 2 * sms ? n_tiles : 2 * sms);  // two CTAs per SM
     const size_t smem = sizeof(EncodeSmem);
     auto run = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        cudaError_t e = set_smem_limit_once(kern, (int)smem, true, dev);
         if (e != cudaSuccess) return e;
         kern<<<grid, kThreads, smem, stream>>>(static_cast<const __nv_bfloat16*>(x), n_tiles,
                                                static_cast<uint8_t*>(codes),
@@ -629,9 +625,7 @@ cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_
                              cudaStream_t stream, const int32_t* dest) {
     if (n_k + n_v == 0) return cudaSuccess;
     int dev = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t err = current_device(&dev, &sms);
     if (err != cudaSuccess) return err;
     const int64_t n = n_k + n_v;
     const int grid = (int)(n < 2 * sms ? n : 2 * sms);
@@ -652,9 +646,7 @@ cudaError_t launch_encode_kv(int k_bits, int v_bits, const void* k_x, int64_t n_
     a.rotate = rotate;
     a.normalize = normalize;
     auto run = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        cudaError_t e = set_smem_limit_once(kern, (int)smem, true, dev);
         if (e != cudaSuccess) return e;
         kern<<<grid, kThreads, smem, stream>>>(a);
         return cudaGetLastError();

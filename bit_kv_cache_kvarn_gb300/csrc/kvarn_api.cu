@@ -10,6 +10,45 @@
 #include "../../include/kvarn.h"
 #include "kvarn_internal.h"
 
+namespace kvarn {
+
+cudaError_t current_device(int* dev, int* sms) {
+    static std::atomic<int> sm_count[kMaxCachedDevices] = {};  // 0: not queried yet
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = *dev >= 0 && *dev < kMaxCachedDevices;
+    if (cached) {
+        const int v = sm_count[*dev].load(std::memory_order_relaxed);
+        if (v > 0) {
+            *sms = v;
+            return cudaSuccess;
+        }
+    }
+    e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev);
+    if (e == cudaSuccess && cached) sm_count[*dev].store(*sms, std::memory_order_relaxed);
+    return e;
+}
+
+cudaError_t set_smem_limit_once(const void* kernel, int bytes, bool max_carveout, int dev) {
+    struct Entry {
+        const void* kernel;
+        int dev, bytes;
+    };
+    static std::mutex mutex;
+    static Entry done[256];  // a few dozen kernels x devices in practice
+    static int n_done = 0;
+    std::lock_guard<std::mutex> lock(mutex);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].kernel == kernel && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess && n_done < 256) done[n_done++] = Entry{kernel, dev, bytes};
+    return e;
+}
+
+}  // namespace kvarn
+
 namespace {
 
 thread_local std::string g_last_error;

@@ -6,7 +6,25 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace kvarn {
+
+// Launch facts cached per device, so that a call makes no driver query after the first one on a
+// device (they cost host time on every call otherwise).
+constexpr int kMaxCachedDevices = 64;
+
+// The calling thread's device and its SM count (queried once per device).
+cudaError_t current_device(int* dev, int* sms);
+
+// Raise the kernel's dynamic shared-memory limit to bytes (and, with max_carveout, prefer the
+// largest shared-memory carveout) unless an earlier call already did so for this kernel (by address)
+// on this device with at least bytes.
+cudaError_t set_smem_limit_once(const void* kernel, int bytes, bool max_carveout, int dev);
+template <typename Kern>
+cudaError_t set_smem_limit_once(Kern kern, int bytes, bool max_carveout, int dev) {
+    return set_smem_limit_once(reinterpret_cast<const void*>(kern), bytes, max_carveout, dev);
+}
 
 size_t encode_smem_bytes();
 cudaError_t read_and_clear_device_error(unsigned int* out);
