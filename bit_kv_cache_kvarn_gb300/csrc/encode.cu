@@ -449,11 +449,13 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
                                 r = v + kRound;
                             }
                         }
-                        const uint32_t c = __float_as_uint(r) & (uint32_t)kLevels;
+                        // r's bits are kRoundBits + code: add them shifted into place and take
+                        // the eight shifted kRoundBits off each word once, below
+                        const uint32_t rb = __float_as_uint(r);
                         if (KIND == KVARN_KIND_K)
-                            packed[k] |= c << (BITS * ii);
+                            packed[k] += rb << (BITS * ii);
                         else
-                            packed[ii] |= c << (BITS * (k ^ kown));
+                            packed[ii] += rb << (BITS * (k ^ kown));
                     }
                 }
             }
@@ -462,6 +464,13 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
             quantise(std::integral_constant<bool, false>());
         else
             quantise(std::integral_constant<bool, true>());
+        // every word received kRoundBits at the eight shifts BITS * n (the sums wrap modulo 2^32)
+        constexpr uint32_t kRoundBits = 0x4B400000u;  // bits of kRound
+        uint32_t offset = 0;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) offset += kRoundBits << (BITS * n);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) packed[q] -= offset;
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
