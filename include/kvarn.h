@@ -225,7 +225,7 @@ kvarn_status kvarn_decode_attention_sink(const kvarn_config* cfg, const void* q_
  *     value a call reads is written earlier in that call).  Calls whose kernels can overlap on the
  *     GPU (different streams without ordering) race on it: serialise them.
  *   - Shapes needing more than KVARN_STATIC_WS_BYTES (see kvarn_decode_workspace_size) return
- *     KVARN_ERR_WORKSPACE before anything is enqueued; e.g. B=16, Hq=32, 256 tiles needs 4.3 MB. */
+ *     KVARN_ERR_WORKSPACE before anything is enqueued; e.g. B=16, Hq=32, Hkv=8, 256 tiles needs 4.4 MiB. */
 #define KVARN_STATIC_WS_BYTES (8u * 1024u * 1024u)
 kvarn_status kvarn_decode_attention_static_ws(
     const kvarn_config* cfg, const void* q_bf16, int B, int Hq, int Hkv, const void* k_codes,
