@@ -1173,11 +1173,21 @@ cudaError_t run_split_g(const DecodeArgs& a, int gh, int grid, cudaStream_t stre
 // Workspace: the partial slots [B][Hq][splits + 1][132] f32, rounded up to 256 bytes.
 DecodePlan plan_decode(int B, int Hq, int Hkv, int max_tiles) {
     DecodePlan p;
-    const long long bound = (long long)B * Hkv * (max_tiles > 0 ? max_tiles : 0);  // full tiles at most
+    const long long units = (long long)B * Hkv;
+    const long long bound = units * (max_tiles > 0 ? max_tiles : 0);  // full tiles at most
     p.piece = kMaxPiece;
     while (p.piece > kMinPieceTiles && bound < kFillWorkers * p.piece) p.piece /= 2;
     p.splits = max_tiles <= 0 ? 1 : (max_tiles + p.piece - 1) / p.piece;
-    p.workspace_bytes = ((size_t)B * Hq * (p.splits + 1) * kWsStride * sizeof(float) + 255) & ~(size_t)255;
+    // The workspace covers every block-table width up to max_tiles, so one sized for the widest
+    // table serves narrower ones (which may take a finer granularity and more slots per tile):
+    // for each finer P the widest table that selects it (bound < 1024 P) gives its slot count.
+    long long ws_splits = p.splits;
+    for (int piece = p.piece / 2; piece >= kMinPieceTiles && units > 0; piece /= 2) {
+        long long m = (2 * kFillWorkers * piece + units - 1) / units - 1;  // widest table with P = piece
+        if (m > max_tiles) m = max_tiles;
+        if (m > 0) ws_splits = ws_splits > (m + piece - 1) / piece ? ws_splits : (m + piece - 1) / piece;
+    }
+    p.workspace_bytes = ((size_t)B * Hq * (ws_splits + 1) * kWsStride * sizeof(float) + 255) & ~(size_t)255;
     return p;
 }
 

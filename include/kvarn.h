@@ -147,11 +147,14 @@ kvarn_status kvarn_dequant(const kvarn_config* cfg, kvarn_kind kind, const void*
                            const void* params, const float* tile_scale, int64_t n_tiles,
                            int original_basis, float* out, kvarn_stream_t stream);
 
-/* Bytes of device workspace kvarn_decode_attention needs for this shape: the split-K partials
- * [B][Hq][S + 1][132] float32 with S = ceil(max_tiles / P) (m, l, 2 pad, o[128] per slot; S = 1
- * when max_tiles is 0), rounded up to a multiple of 256.  P, the piece granularity, is 16, halved
- * (down to 2) while B * Hkv * max_tiles < 512 * P: calls with few tiles are cut into shorter pieces
- * for more parallel workers.  Returns 0 for an invalid shape.  (The split-K decomposition and its
+/* Bytes of device workspace kvarn_decode_attention needs for this shape and for every narrower
+ * block table (max_tiles' <= max_tiles, same B, Hq, Hkv), so one workspace sized for the widest
+ * table serves all calls; never smaller for a larger max_tiles.  A call with table width m uses the
+ * split-K partials [B][Hq][S + 1][132] float32, S = ceil(m / P) (m, l, 2 pad, o[128] per slot; S = 1
+ * when m is 0), where P, the piece granularity, is 16, halved (down to 2) while B * Hkv * m < 512 * P:
+ * calls with few tiles are cut into shorter pieces for more parallel workers.  The size is the
+ * largest such slot array over m <= max_tiles, rounded up to a multiple of 256.  Returns 0 for an
+ * invalid shape.  (The split-K decomposition and its
  * log-sum-exp merge are this library's; the pages only say that attention reads the cache.) */
 size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int Hkv,
                                    int max_tiles);

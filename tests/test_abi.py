@@ -167,23 +167,61 @@ def test_workspace_plan(lib):
 
     cfg = _cfg()
 
-    def expected(B, Hq, Hkv, max_tiles):
-        # piece granularity P: 16, halved (down to 2) while B Hkv max_tiles < 512 P; partial slots:
-        # one per P-tile block plus one; (m, l, 2 pad, o[128]) floats per slot, rounded up to 256 bytes
+    def piece(units, m):
+        # piece granularity P: 16, halved (down to 2) while B Hkv (table width) < 512 P
         p = 16
-        while p > 2 and B * Hkv * max_tiles < 512 * p:
+        while p > 2 and units * m < 512 * p:
             p //= 2
-        up = lambda x: (x + 255) // 256 * 256
-        slots = max(1, -(-max_tiles // p)) + 1
-        return up(B * Hq * slots * 132 * 4)
+        return p
+
+    def expected(B, Hq, Hkv, max_tiles):
+        # enough for every table width up to max_tiles (a narrower table may take a finer P), 256-byte
+        # multiple: the widest width of each finer granularity gives its largest slot count
+        units = B * Hkv
+        P = piece(units, max_tiles)
+        s = max(1, -(-max_tiles // P))
+        q = P // 2
+        while q >= 2 and units > 0:
+            m = min(max_tiles, -(-1024 * q // units) - 1)
+            if m > 0:
+                s = max(s, -(-m // q))
+            q //= 2
+        return (B * Hq * (s + 1) * 528 + 255) // 256 * 256
 
     assert kv.kvarn_decode_workspace_size(cfg, 16, 32, 8, 256) == expected(16, 32, 8, 256)
     assert kv.kvarn_decode_workspace_size(cfg, 4, 40, 10, 1024) == expected(4, 40, 10, 1024)
     assert kv.kvarn_decode_workspace_size(cfg, 1, 4, 1, 0) == expected(1, 4, 1, 0)
     # small calls take finer pieces: B = 1, 8 kv heads, 32 tiles -> P = 2, 17 slots per head
     assert kv.kvarn_decode_workspace_size(cfg, 1, 32, 8, 32) == expected(1, 32, 8, 32) == 32 * 17 * 528
-    assert expected(2, 32, 8, 256) == 2 * 32 * (256 // 8 + 1) * 528  # 4096 tiles: P = 8
+    # 2 x 8 units x 256 tiles = 4096 stream tiles: P = 8 (33 slots), but a 255-tile table takes P = 4
+    # (65 slots), so the workspace holds 65
+    assert expected(2, 32, 8, 256) == 2 * 32 * 65 * 528
+    assert kv.kvarn_decode_workspace_size(cfg, 2, 32, 8, 256) == expected(2, 32, 8, 256)
     assert kv.kvarn_decode_workspace_size(cfg, 1, 6, 4, 1) == 0
+
+
+def test_workspace_covers_every_narrower_table(lib):
+    # brute force: a workspace sized for max_tiles serves any table width m <= max_tiles, and it
+    # never shrinks as max_tiles grows
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    cfg = _cfg()
+
+    def needed(B, Hq, Hkv, m):
+        units, p = B * Hkv, 16
+        while p > 2 and units * m < 512 * p:
+            p //= 2
+        return B * Hq * (max(1, -(-m // p)) + 1) * 528
+
+    for B, Hkv in ((1, 1), (1, 8), (2, 8), (3, 5), (16, 8)):
+        Hq = 2 * Hkv
+        prev, worst = 0, 0
+        for m in range(0, 1200):
+            worst = max(worst, needed(B, Hq, Hkv, m))
+            got = kv.kvarn_decode_workspace_size(cfg, B, Hq, Hkv, m)
+            assert got >= worst, (B, Hkv, m, got, worst)
+            assert got >= prev, (B, Hkv, m)
+            prev = got
 
 
 def test_append_validation_needs_no_gpu(lib):

@@ -113,8 +113,8 @@ def test_piece_granularities_with_ragged_lengths(kv, B, hkv, lens_tiles, piece):
     lens = [t * 128 + (37 * i) % 128 for i, t in enumerate(lens_tiles)]
     c = build_cache(kv, cfg, B, hkv, lens, seed=31 + piece)
     hq = 2 * hkv
-    slots = -(-c["nt"] // piece) + 1
-    assert kv.kvarn_decode_workspace_size(cfg, B, hq, hkv, c["nt"]) == -(-(B * hq * slots * 528) // 256) * 256
+    slots = -(-c["nt"] // piece) + 1  # this width's partial slots at granularity P
+    assert kv.kvarn_decode_workspace_size(cfg, B, hq, hkv, c["nt"]) >= B * hq * slots * 528
     q = kv.synthetic.queries(31, B, hq, device="cuda")
     gpu = run_gpu(kv, cfg, q, hkv, c, 0.09)
     print(f"P = {piece} worst rel-L2", check(gpu, oracle_out(cfg, q, hkv, c, 0.09)))
