@@ -54,7 +54,7 @@ constexpr int kIdRing = 32;                // tile-id ring of a worker
 constexpr int kIdBatch = 16;               // tile ids are fetched 16 at a time, one batch ahead
 constexpr int kWsStride = 132;  // floats per (sequence, query head, split): m, l, pad, pad, o[128]
 constexpr uint32_t kTmemCols = 256;         // worker w: A (64) and D (4 partials x 16) at 128 w
-constexpr uint32_t kBBytes = 256 * 16 * 2;  // one B operand: K = 256 x N = 16 fp16, N-contiguous
+constexpr uint32_t kBBytes = 128 * 16 * 2;  // one B operand: K = 128 x N = 16 fp16, N-contiguous
 constexpr uint32_t kBKStride = 256, kBNStride = 128;  // core-matrix strides of B along K and N
 // Lazy maximum: keep the running max while no score exceeds it by more than kLazy (log2 units), so
 // p <= 2^kLazy; with S1 <= 256, p S1 kWScale <= 2^15 fits fp16 while small terms stay normal.
