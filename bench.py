@@ -332,6 +332,114 @@ def run_latency():
                       "heads": f"{DEC_HQ}q/{DEC_HKV}kv", "preset": "kvarn_k2v2_g128", "results": res}), flush=True)
 
 
+def run_configs():
+    """The other workloads, timed as single calls (CUDA events, 256 MiB L2 flush before each):
+    the encode of 512 K + 512 V blocks (64 sequences x 8 kv heads, Qwen3-4B shaped, seed 1) under
+    both presets, and decode attention over the Phi-4 shaped ragged long-context cache (40q/10kv
+    heads, batch 4, lengths U[65536, 131072] from seed 3, 4-bit K / 2-bit V, the last len % 128
+    tokens of each sequence in the bf16 tails).  Rates use the algorithmic bytes of each call."""
+    import torch
+
+    import bit_kv_cache_kvarn_gb300 as kv
+
+    kv.load()
+    dev = torch.device("cuda", 0)
+    hbm, src = peaks()
+    flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.add_(1.0)
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c) * 1000)
+        return statistics.mean(ts)
+
+    res = {}
+    n_enc = ENC_SEQ * ENC_HKV
+    ek, ev = kv.synthetic.outlier_kv(1, n_enc, 128, device=dev)
+    ek, ev = ek.reshape(n_enc, 128, 128), ev.reshape(n_enc, 128, 128)
+    for preset in ("kvarn_k4v2_g128", "kvarn_k2v2_g128"):
+        cfg = kv.kvarn_config_from_preset(preset)
+        outs = []
+        for bits in (cfg.k_bits, cfg.v_bits):
+            outs += [torch.empty(n_enc, 128 * 16 * bits, dtype=torch.uint8, device=dev),
+                     torch.empty(n_enc, 512, dtype=torch.uint8, device=dev),
+                     torch.empty(n_enc, dtype=torch.float32, device=dev)]
+        us = timed(lambda: kv.kvarn_encode_kv_blocks(cfg, ek, ev, *outs), 200)
+        e_in, e_out = enc_bytes(n_enc, cfg.k_bits, cfg.v_bits)
+        tflops = 2 * n_enc * 128 * 128 * ENC_FLOPS_PER_ELEMENT / (us * 1e-6) / 1e12
+        res[f"encode 512 K + 512 V blocks, {preset}"] = {
+            "us": round(us, 2), "bytes": e_in + e_out, "gbs": round((e_in + e_out) / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round((e_in + e_out) / (us * 1e-6) / 1e9 / hbm, 4),
+            "alu_frac": round(tflops / FP32_PEAK_TFLOPS, 4)}
+    del ek, ev
+
+    cfg = kv.kvarn_config_from_preset("kvarn_k4v2_g128")
+    B, Hq, Hkv = 4, 40, 10
+    lens = kv.synthetic.ragged_lengths(3, B, 65536, 131072)
+    pools, table, (kt, vt), seq_lens, nt = build_ragged_cache(kv, cfg, B, Hkv, lens, 3, dev)
+    q = kv.synthetic.queries(3, B, Hq, device=dev)
+    ws = torch.empty(kv.kvarn_decode_workspace_size(cfg, B, Hq, Hkv, nt), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, Hq, 128, device=dev)
+    us = timed(lambda: kv.kvarn_decode_attention(cfg, q, Hkv, *pools["k"], *pools["v"], table, seq_lens, kt, vt,
+                                                 1 / math.sqrt(128), ws, out, seq_lens_host=lens), 200)
+    tile = (128 * 16 * cfg.k_bits + 516) + (128 * 16 * cfg.v_bits + 516)
+    cache = sum(Hkv * ((L // 128) * tile + (L % 128) * 128 * 2 * 2) for L in lens)
+    nbytes = cache + B * Hq * 128 * 2 + B * Hq * 128 * 4
+    res["decode B=4, 40q/10kv heads, ragged 64k-128k context, kvarn_k4v2_g128"] = {
+        "us": round(us, 2), "lens": lens, "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+        "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4),
+        "kv_tokens_per_s": round(Hkv * sum(lens) / (us * 1e-6), 1)}
+    assert kv.kvarn_device_error() == 0
+    print(json.dumps({"impl": "configs", "unit": "us per call", "hbm_peak_gbs": hbm, "peak_source": src,
+                      "l2": "flushed (256 MiB read+write) before every call", "results": res}), flush=True)
+
+
+def build_ragged_cache(kv, cfg, B, Hkv, lens, seed, device):
+    """Encode every full 128-token block of each (sequence, kv head) of length lens[b] into pools
+    whose tile ids are scattered by a seeded permutation; the last len % 128 tokens go to bf16
+    tails.  Returns pools, block table [B, Hkv, nt], (k_tail, v_tail), seq_lens, nt."""
+    import torch
+
+    U = B * Hkv
+    nt = max(lens) // 128 + 1
+    k, v = kv.synthetic.outlier_kv(seed, U, nt * 128, device=device)
+    pools = {}
+    for kind, name, x in ((kv.KVARN_KIND_K, "k", k), (kv.KVARN_KIND_V, "v", v)):
+        bits = cfg.k_bits if name == "k" else cfg.v_bits
+        codes = torch.empty(U * nt, 128 * 16 * bits, dtype=torch.uint8, device=device)
+        params = torch.empty(U * nt, 512, dtype=torch.uint8, device=device)
+        scale = torch.empty(U * nt, dtype=torch.float32, device=device)
+        kv.kvarn_encode_blocks(cfg, kind, x.reshape(-1, 128, 128), codes, params, scale)
+        pools[name] = (codes, params, scale)
+    perm = kv.synthetic.tile_permutation(seed, U * nt, device=device)
+    for name in ("k", "v"):
+        c, p, s = pools[name]
+        c2, p2, s2 = torch.empty_like(c), torch.empty_like(p), torch.empty_like(s)
+        c2[perm], p2[perm], s2[perm] = c, p, s
+        pools[name] = (c2, p2, s2)
+    table = perm.to(torch.int32).reshape(B, Hkv, nt).contiguous()
+    tails = []
+    for x in (k, v):
+        t = torch.zeros(B, Hkv, 128, 128, dtype=torch.bfloat16, device=device)
+        xr = x.reshape(B, Hkv, nt * 128, 128)
+        for b, L in enumerate(lens):
+            full = L // 128 * 128
+            t[b, :, :L - full] = xr[b, :, full:L]
+        tails.append(t)
+    del k, v
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device=device)
+    torch.cuda.synchronize()
+    return pools, table, tuple(tails), seq_lens, nt
+
+
 def run_append_timing():
     """Time kvarn_append_tokens on the decode workload's shape (B 16 x 8 kv heads): one token per
     sequence per step (1 in 128 steps completes a block), and 128 tokens per sequence (every
@@ -597,6 +705,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=32768, help="decode context (profiling runs only)")
     ap.add_argument("--append-timing", action="store_true",
                     help="time kvarn_append_tokens on the decode shape instead of the step")
+    ap.add_argument("--configs", action="store_true",
+                    help="time the K4/V2 and K2/V2 encodes and the ragged long-context K4/V2 decode")
     ap.add_argument("--latency", action="store_true",
                     help="time single decode calls at small serving shapes instead of the step")
     ap.add_argument("--diagnostics", action="store_true",
@@ -610,6 +720,8 @@ def main():
         run_diagnostics()
     elif args.append_timing:
         run_append_timing()
+    elif args.configs:
+        run_configs()
     elif args.latency:
         run_latency()
     elif args.impl == "reference":
