@@ -983,9 +983,21 @@ __device__ __forceinline__ float merge_warp_parts(float4 acc, float (*part)[kTil
 //      a time: thread t scores token t (its whole row at once), one online-softmax update per chunk,
 //      and the p-weighted V rows again spread over the warps;
 //   3. normalise by l.
-// Every load of a phase is independent of the others, so a chunk costs a few memory round trips
-// rather than one per token.
-__global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
+// The kernel is a chain of dependent steps behind the split grid, so its loads are issued early:
+// right after the wait, one round trip brings each thread's slot (m, l), each warp's o rows of the
+// first 4 x kPreSlots = 20 slots (17 at the usual piece sizes) and the query; later loads are only for
+// slots beyond those.  At <= 128 registers four CTAs fit on an SM, so B 16 x 32 heads is one wave.
+constexpr int kPreSlots = 5;  // o rows prefetched per warp: slots warp, warp + 4, ..., warp + 16
+
+__device__ __forceinline__ float4 fma4(float4 v, float w, float4 acc) {
+    acc.x = fmaf(v.x, w, acc.x);
+    acc.y = fmaf(v.y, w, acc.y);
+    acc.z = fmaf(v.z, w, acc.z);
+    acc.w = fmaf(v.w, w, acc.w);
+    return acc;
+}
+
+__global__ void __launch_bounds__(kTile, 4) decode_merge_kernel(DecodeArgs a) {
     __shared__ __align__(16) float s_q[kTile];     // scaled query, original basis
     __shared__ __align__(16) float s_w[kTile];     // slot weights / token probabilities of a chunk
     __shared__ __align__(16) float s_part[4][kTile];
@@ -1000,13 +1012,37 @@ __global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
     const int nt = n_full_tiles(len, a.full_tail);
     const int tail = len - nt * kTile;  // 0..127, or 1..128 with the full window
     const int n_sink = max(0, min(a.sink_len, a.seq_lens[b]));
+    const int n_tok = n_sink + tail;
+    const size_t tb = ((size_t)b * a.Hkv + kvh) * kTile * kTile;
     const float* base = slot_ptr(a, b, hq, 0);
     // the slots this (sequence, head) has: one per P-tile block and the unit-entry slot
     const int n_slots = nt > 0 ? (nt + a.piece - 1) / a.piece + 1 : 0;
     auto slot_of = [&](int i) { return i + 1 == n_slots ? a.splits : i; };
+    // row of unquantised token t (sink first, then tail)
+    auto k_row = [&](int t) {
+        const bool in_sink = t < n_sink;
+        return reinterpret_cast<const uint4*>((in_sink ? a.k_sink : a.k_tail) + tb +
+                                              (size_t)(in_sink ? t : t - n_sink) * kTile);
+    };
 
-    float mloc = -INFINITY;
-    for (int i = c; i < n_slots; i += kTile) mloc = fmaxf(mloc, __ldcg(base + slot_of(i) * kWsStride));
+    // ---- the first round trip ----
+    float m0 = -INFINITY, l0 = 0.f;
+    if (c < n_slots) {
+        m0 = __ldcg(base + slot_of(c) * kWsStride);
+        l0 = __ldcg(base + slot_of(c) * kWsStride + 1);
+    }
+    float4 pre[kPreSlots];
+#pragma unroll
+    for (int q = 0; q < kPreSlots; ++q) {
+        const int j = warp + 4 * q;
+        // rows of empty slots hold whatever the workspace held: loaded, never used
+        pre[q] = j < n_slots ? __ldcg(reinterpret_cast<const float4*>(base + slot_of(j) * kWsStride + 4) + lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float qc = n_tok > 0 ? __bfloat162float(a.q[((size_t)b * a.Hq + hq) * kTile + c]) * a.qscale : 0.f;
+
+    float mloc = m0;
+    for (int i = c + kTile; i < n_slots; i += kTile) mloc = fmaxf(mloc, __ldcg(base + slot_of(i) * kWsStride));
     float mmax = merge_max(mloc, s_red);
     float l = 0.f, o = 0.f;
     if (mmax != -INFINITY) {  // uniform over the CTA
@@ -1016,25 +1052,32 @@ __global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
             const int i = k0 + c;
             float w = 0.f;
             if (i < n_slots) {
-                const float m = __ldcg(base + slot_of(i) * kWsStride);
+                const float m = k0 == 0 ? m0 : __ldcg(base + slot_of(i) * kWsStride);
                 if (m != -INFINITY) {  // an empty slot (its o is not written) weighs 0
                     w = fast_exp2(m - mmax);
-                    lloc = fmaf(__ldcg(base + slot_of(i) * kWsStride + 1), w, lloc);
+                    lloc = fmaf(k0 == 0 ? l0 : __ldcg(base + slot_of(i) * kWsStride + 1), w, lloc);
                 }
             }
             __syncthreads();  // s_w is free again
             s_w[c] = w;
             __syncthreads();
             const int n_c = min(kTile, n_slots - k0);
+            int j = warp;
+            if (k0 == 0) {
+#pragma unroll
+                for (int q = 0; q < kPreSlots; ++q, j += 4) {
+                    if (j < n_c) {
+                        const float wj = s_w[j];
+                        if (wj != 0.f) acc = fma4(pre[q], wj, acc);
+                    }
+                }
+            }
 #pragma unroll 4
-            for (int j = warp; j < n_c; j += 4) {
+            for (; j < n_c; j += 4) {
                 const float wj = s_w[j];
                 if (wj == 0.f) continue;
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(base + slot_of(k0 + j) * kWsStride + 4) + lane);
-                acc.x = fmaf(v.x, wj, acc.x);
-                acc.y = fmaf(v.y, wj, acc.y);
-                acc.z = fmaf(v.z, wj, acc.z);
-                acc.w = fmaf(v.w, wj, acc.w);
+                acc = fma4(__ldcg(reinterpret_cast<const float4*>(base + slot_of(k0 + j) * kWsStride + 4) + lane), wj,
+                           acc);
             }
         }
         l = merge_sum(lloc, s_red);
@@ -1042,18 +1085,14 @@ __global__ void __launch_bounds__(kTile) decode_merge_kernel(DecodeArgs a) {
         if (a.rotate) o = fwht128_block(o, s_w) * kInvSqrt128;
     }
 
-    const int n_tok = n_sink + tail;
     if (n_tok > 0) {
-        s_q[c] = __bfloat162float(a.q[((size_t)b * a.Hq + hq) * kTile + c]) * a.qscale;
-        const size_t tb = ((size_t)b * a.Hkv + kvh) * kTile * kTile;
+        s_q[c] = qc;
         __syncthreads();
         for (int t0 = 0; t0 < n_tok; t0 += kTile) {
             const int t = t0 + c;
             float sc = -INFINITY;
             if (t < n_tok) {
-                const bool in_sink = t < n_sink;
-                const uint4* kr = reinterpret_cast<const uint4*>((in_sink ? a.k_sink : a.k_tail) + tb +
-                                                                 (size_t)(in_sink ? t : t - n_sink) * kTile);
+                const uint4* kr = k_row(t);
                 uint4 raw[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) raw[i] = __ldg(kr + i);
