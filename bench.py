@@ -66,6 +66,15 @@ def dec_bytes(k_bits=2, v_bits=2):
     return cache, q, out
 
 
+def ragged_dec_bytes(lens, Hq, Hkv, k_bits, v_bits):
+    """Algorithmic bytes of one decode call over sequences of lengths `lens`: each (sequence, kv
+    head) reads its L // 128 packed K and V tiles (codes, 512 B of parameters and a 4-byte factor
+    each) and its L % 128 bf16 tail tokens of K and V; plus the bf16 queries and fp32 outputs."""
+    tile = (128 * 16 * k_bits + 516) + (128 * 16 * v_bits + 516)
+    cache = sum(Hkv * ((L // 128) * tile + (L % 128) * 128 * 2 * 2) for L in lens)
+    return cache, len(lens) * Hq * 128 * 2, len(lens) * Hq * 128 * 4
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_kvarn_gb300", "csrc")
@@ -390,9 +399,7 @@ def run_configs():
     out = torch.empty(B, Hq, 128, device=dev)
     us = timed(lambda: kv.kvarn_decode_attention(cfg, q, Hkv, *pools["k"], *pools["v"], table, seq_lens, kt, vt,
                                                  1 / math.sqrt(128), ws, out, seq_lens_host=lens), 200)
-    tile = (128 * 16 * cfg.k_bits + 516) + (128 * 16 * cfg.v_bits + 516)
-    cache = sum(Hkv * ((L // 128) * tile + (L % 128) * 128 * 2 * 2) for L in lens)
-    nbytes = cache + B * Hq * 128 * 2 + B * Hq * 128 * 4
+    nbytes = sum(ragged_dec_bytes(lens, Hq, Hkv, cfg.k_bits, cfg.v_bits))
     res["decode B=4, 40q/10kv heads, ragged 64k-128k context, kvarn_k4v2_g128"] = {
         "us": round(us, 2), "lens": lens, "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
         "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4),

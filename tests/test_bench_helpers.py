@@ -33,6 +33,18 @@ def test_decode_bytes_of_the_bench_call():
     assert cache == 16 * 8 * 32768 * 72 + 16 * 8 * 256 * 8
 
 
+def test_ragged_decode_bytes():
+    # the bench cache through the ragged formula: the same bytes as the fixed-length count
+    assert bench.ragged_dec_bytes([32768] * 16, 32, 8, 2, 2) == bench.dec_bytes()
+    # one sequence of 2 full tiles + 5 tail tokens, 4-bit K / 2-bit V, 40q/10kv heads, by hand:
+    # per kv head 2 x ((8192 + 512 + 4) + (4096 + 512 + 4)) B of tiles + 5 x 128 x 2 B x 2 of tails
+    cache, q, out = bench.ragged_dec_bytes([2 * 128 + 5], 40, 10, 4, 2)
+    assert cache == 10 * (2 * (8708 + 4612) + 5 * 512) == 292_000
+    assert q == 40 * 128 * 2 and out == 40 * 128 * 4
+    # an empty sequence reads nothing of the cache
+    assert bench.ragged_dec_bytes([0], 8, 2, 2, 2)[0] == 0
+
+
 def test_ncu_traffic_only_for_the_captured_sources(tmp_path, monkeypatch):
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         committed = json.load(f)
