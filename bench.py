@@ -241,10 +241,12 @@ def max_over_ranks(values, world, device):
     return [float(x) for x in t]
 
 
-def job_us_per_step(step_ms_max, world):
-    """N replicas each finish one step within the max-over-ranks time: the whole job's time per
-    step is that time divided by N (weak scaling, replicas only)."""
-    return step_ms_max * 1000.0 / world
+def replica_step_rates(step_ms_max, world):
+    """(us per step, replica steps per second of the whole job).  Each of the N replicas runs one
+    full step of the workload within the max-over-ranks time, so the per-step time stays that of
+    one rank (weak scaling, replicas only) while the job completes N steps in that time."""
+    us = step_ms_max * 1000.0
+    return us, world / (step_ms_max * 1e-3)
 
 
 def run_diagnostics():
@@ -656,7 +658,7 @@ def run_gpu(args):
         dec_alg = d_cache + d_q + d_out
         dec_gbs = dec_alg / (dec_ms_m * 1e-3) / 1e9
         traffic = ncu_traffic("kvarn_decode_attention")
-        value_us = job_us_per_step(step_ms, world)
+        value_us, job_steps_per_s = replica_step_rates(step_ms, world)
         line = {
             "metric": METRIC, "value": round(value_us, 2), "unit": "us/step", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -665,6 +667,7 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD, "preset": "kvarn_k2v2_g128", "sinkhorn_iters": 8,
                        "l2": "flushed (256 MiB read+write) before every step; decode cache 302 MB > L2",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
+            "job_steps_per_s": round(job_steps_per_s, 1),
             "encode": {"us": round(enc_ms_m * 1000, 2), "gbs_bf16_input": round(enc_in_gbs, 1),
                        "gbs_read_plus_write": round(enc_gbs, 1), "hbm_frac": round(enc_gbs / hbm, 4),
                        "bytes_per_step": e_in + e_out, "launches_per_step": 1,
@@ -683,7 +686,7 @@ def run_gpu(args):
                          "achieved": round(dec_gbs, 1), "peak": hbm, "peak_source": src,
                          "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
                          "traffic": traffic},
-            "e2e": {"value": round(job_us_per_step(e2e_ms, world), 2), "unit": "us/step",
+            "e2e": {"value": round(replica_step_rates(e2e_ms, world)[0], 2), "unit": "us/step",
                     "h2d_bytes_per_step": 2 * ek.numel() * 2 + q.numel() * 2,
                     "d2h_bytes_per_step": out.numel() * 4,
                     "schedule": "K/V upload on a copy stream during the decode; encode after it; "

@@ -1,5 +1,5 @@
 """The bench's replica bookkeeping over two CPU ranks (gloo): the timings reported are the maximum
-over the ranks and the whole-job time per step divides it by the number of replicas."""
+over the ranks; the per-step time stays one rank's and the job's step rate counts every replica."""
 import os
 import socket
 
@@ -25,7 +25,7 @@ def _rank_main(rank, world, port, root, q):
         import bench
 
         got = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.25 * (rank + 1)], world, "cpu")
-        q.put((rank, got, bench.job_us_per_step(got[0], world)))
+        q.put((rank, got, bench.replica_step_rates(got[0], world)))
         dist.barrier()
         dist.destroy_process_group()
     except Exception as e:  # report instead of leaving the parent waiting
@@ -46,12 +46,15 @@ def test_max_over_two_gloo_ranks():
         assert p.exitcode == 0
     for rank, got, job in results:
         assert got == [2.0, 10.0, 0.5]
-        assert job == pytest.approx(1000.0)
+        us, rate = job
+        assert us == pytest.approx(2000.0)  # the slowest rank's 2 ms step, not divided by N
+        assert rate == pytest.approx(1000.0)  # two replica steps every 2 ms
 
 
 def test_single_rank_needs_no_process_group():
     import bench
 
     assert bench.max_over_ranks([3.0, 4.0], 1, "cpu") == [3.0, 4.0]
-    assert bench.job_us_per_step(0.25, 1) == pytest.approx(250.0)
+    us, rate = bench.replica_step_rates(0.25, 1)
+    assert us == pytest.approx(250.0) and rate == pytest.approx(4000.0)
     assert torch.distributed.is_initialized() is False
