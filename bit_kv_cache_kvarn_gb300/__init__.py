@@ -26,10 +26,14 @@ PARAM_BYTES = 512
 TILE = 128
 
 
+KVARN_ERR_TIMEOUT = 5
+
+
 class KvarnError(RuntimeError):
-    def __init__(self, status: int, msg: str):
+    def __init__(self, status: int, msg: str, code: int | None = None):
         super().__init__(f"{msg} (status {status})")
         self.status = status
+        self.code = code  # kvarn_device_error's bits, for KVARN_ERR_TIMEOUT
 
 
 class kvarn_config(ctypes.Structure):
@@ -66,6 +70,7 @@ _SIGNATURES = {
                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                                                 _vp, _vp, ctypes.c_float, _vp, _vp]),
     "kvarn_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
+    "kvarn_check_bounded_wait": (_i32, [ctypes.c_uint32, _vp]),
     "kvarn_append_workspace_size": (_sz, [_i32, _i32]),
     "kvarn_append_tokens": (_i32, [ctypes.POINTER(kvarn_config), _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
@@ -282,9 +287,20 @@ def kvarn_decode_attention_static_ws(cfg: kvarn_config, q, Hkv: int, k_codes, k_
 
 
 def kvarn_device_error() -> int:
+    """The device error bits (read and cleared).  Raises KvarnError (status KVARN_ERR_TIMEOUT, the
+    bits in .code) when a bounded device wait gave up."""
     v = ctypes.c_uint32(0)
-    _check(load().kvarn_device_error(ctypes.byref(v)))
+    lib = load()
+    st = lib.kvarn_device_error(ctypes.byref(v))
+    if st == KVARN_ERR_TIMEOUT:
+        raise KvarnError(st, lib.kvarn_last_error().decode(), code=int(v.value))
+    _check(st)
     return int(v.value)
+
+
+def kvarn_check_bounded_wait(limit_us: int, stream=None):
+    """Enqueue the self-check kernel whose bounded wait gives up after limit_us microseconds."""
+    _check(load().kvarn_check_bounded_wait(int(limit_us), _stream(stream)))
 
 
 def kvarn_status_string(status: int) -> str:

@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvarn.so")
-SOURCES = ["kvarn_api.cu", "encode.cu", "dequant.cu", "decode_attn.cu", "append.cu"]
+SOURCES = ["kvarn_api.cu", "encode.cu", "dequant.cu", "decode_attn.cu", "append.cu", "bounded_wait.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]

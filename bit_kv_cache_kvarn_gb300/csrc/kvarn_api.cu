@@ -320,7 +320,20 @@ kvarn_status kvarn_device_error(uint32_t* code_out) {
     unsigned int x = 0;
     e = kvarn::read_and_clear_append_error(&x);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
-    *code_out = v | (w << 1) | (x << 2);
+    unsigned int y = 0;
+    e = kvarn::read_and_clear_selftest_error(&y);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    *code_out = v | (w << 1) | (x << 2) | (y << 3);
+    if (*code_out & KVARN_DEVICE_TIMEOUT_BITS)
+        return fail(KVARN_ERR_TIMEOUT, "a bounded device wait gave up (device error bits 0x%x)", *code_out);
+    return ok();
+}
+
+kvarn_status kvarn_check_bounded_wait(uint32_t limit_us, kvarn_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(KVARN_ERR_INVALID_ARG, "limit_us = %u outside 1..1000000", limit_us);
+    cudaError_t e = kvarn::launch_bounded_wait_check(limit_us, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "bounded-wait check launch");
     return ok();
 }
 
@@ -442,6 +455,7 @@ const char* kvarn_status_string(kvarn_status status) {
         case KVARN_ERR_UNSUPPORTED: return "KVARN_ERR_UNSUPPORTED: valid but not implemented";
         case KVARN_ERR_CUDA: return "KVARN_ERR_CUDA: a CUDA call or kernel launch failed";
         case KVARN_ERR_WORKSPACE: return "KVARN_ERR_WORKSPACE: workspace too small";
+        case KVARN_ERR_TIMEOUT: return "KVARN_ERR_TIMEOUT: a bounded device wait gave up";
     }
     return "unknown kvarn_status";
 }

@@ -89,11 +89,12 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for the mbarrier phase with the given parity.  Bounded: gives up after kWaitNs of wall time
+// Wait for the mbarrier phase with the given parity.  Bounded: gives up after limit_ns of wall time
 // (or kSpinLimit polls), sets *err_word and returns false; once *err_word is set by any thread of
 // the grid, every later wait returns false at once, so a stuck kernel ends within about a second.
 constexpr uint64_t kWaitNs = 1000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err_word) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* err_word,
+                                              uint64_t limit_ns) {
     const uint32_t addr = smem_addr(bar);
     uint64_t t0 = 0;
     for (long long i = 0; i < kSpinLimit; ++i) {
@@ -108,11 +109,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
             if (*reinterpret_cast<volatile unsigned int*>(err_word)) return false;
             const uint64_t t = global_ns();
             if (i == 0) t0 = t;
-            else if (t - t0 > kWaitNs) break;
+            else if (t - t0 > limit_ns) break;
         }
     }
     atomicOr(err_word, kErrTmaTimeout);
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err_word) {
+    return mbar_wait_for(bar, parity, err_word, kWaitNs);
 }
 
 // After a give-up: wait (bounded by time only) for a copy this CTA issued, so it never exits with a

@@ -81,4 +81,8 @@ cudaError_t launch_append(const AppendArgs& a, int B, int k_bits, int v_bits, in
                           void* v_params, float* v_scale, cudaStream_t stream);
 cudaError_t read_and_clear_append_error(unsigned int* out);
 
+// Self-check: one kernel whose bounded mbarrier wait runs out after limit_us (see bounded_wait.cu).
+cudaError_t launch_bounded_wait_check(uint32_t limit_us, cudaStream_t stream);
+cudaError_t read_and_clear_selftest_error(unsigned int* out);
+
 }  // namespace kvarn

@@ -72,7 +72,8 @@ typedef enum {
     KVARN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or enum is out of range */
     KVARN_ERR_UNSUPPORTED = 2, /* a valid but unimplemented combination (e.g. 3-bit codes) */
     KVARN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-    KVARN_ERR_WORKSPACE = 4    /* the workspace passed is smaller than required */
+    KVARN_ERR_WORKSPACE = 4,   /* the workspace passed is smaller than required */
+    KVARN_ERR_TIMEOUT = 5      /* a device-side wait gave up (reported by kvarn_device_error) */
 } kvarn_status;
 
 /* Which cache a tile belongs to; selects the group axis (K: channel, V: token). */
@@ -223,7 +224,10 @@ kvarn_status kvarn_decode_attention_sink(const kvarn_config* cfg, const void* q_
  * offers no scratch, or a latency-critical loop that must not hit cudaMalloc's implicit
  * synchronisation.  Nothing is allocated: no cudaMalloc/cudaFree, no allocating library routine.
  *   - The first call on a device, with that device current, looks up the array's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.  The
+ *     cached address belongs to the device's primary context: it does not survive
+ *     cudaDeviceReset() (or any teardown of that context), after which the array may sit
+ *     elsewhere -- a process that resets a device must not call this entry point on it again.
  *   - All calls on a device share the one array and it keeps the previous call's contents (every
  *     value a call reads is written earlier in that call).  Calls whose kernels can overlap on the
  *     GPU (different streams without ordering) race on it: serialise them.
@@ -270,9 +274,26 @@ kvarn_status kvarn_append_tokens(const kvarn_config* cfg, int B, int Hkv, const 
 /* Reads and clears the device-side error words of the current device, after synchronising it.
  * Bit 1 (value 1): an encoder TMA bulk copy did not complete within its bounded wait (the affected
  * tiles are left unwritten).  Bit 2 (value 2): a decode wait gave up.  Bit 3 (value 4): an append
- * found no block-table slot for a completed block.  *code_out = 0 means no such event.
+ * found no block-table slot for a completed block.  Bit 4 (value 8): the wait of
+ * kvarn_check_bounded_wait gave up.  *code_out = 0 means no such event.
+ * Kernels cannot return a status to the call that enqueued them (that call has returned long
+ * before they run), so a device wait that gives up sets its bit, ends its kernel normally -- the
+ * CUDA context stays usable -- and is reported here: the call returns KVARN_ERR_TIMEOUT when any
+ * timeout bit (KVARN_DEVICE_TIMEOUT_BITS) was set, KVARN_OK otherwise (bit 3 alone is reported in
+ * *code_out with KVARN_OK); *code_out is filled in both cases.  The bits stay set until read: until
+ * then every bounded wait of the kernel family that set one gives up at once.
  * (A library diagnostic; the pages have no counterpart.) */
+#define KVARN_DEVICE_TIMEOUT_BITS 0xBu
 kvarn_status kvarn_device_error(uint32_t* code_out);
+
+/* Self-check of the bounded device waits (a library diagnostic; the pages have no counterpart).
+ * Enqueues one small kernel whose mbarrier wait cannot complete (it expects 16 bytes that no copy
+ * delivers) and therefore gives up after limit_us microseconds (1..1000000): the kernel sets bit 4
+ * of the device error word and ends normally.  A following kvarn_device_error returns
+ * KVARN_ERR_TIMEOUT with bit 4 set, and the device stays usable.  No fault, trap or hang is
+ * involved; this is how the failure path of every bounded wait in the library is tested.
+ * Errors: KVARN_ERR_INVALID_ARG for limit_us outside 1..1000000. */
+kvarn_status kvarn_check_bounded_wait(uint32_t limit_us, kvarn_stream_t stream);
 
 /* Static text for a status code. */
 const char* kvarn_status_string(kvarn_status status);

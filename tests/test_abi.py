@@ -58,8 +58,9 @@ def test_presets_and_sizes(lib):
         kv.kvarn_config_from_preset("kvarn_k3v3")
     assert kv.kvarn_tile_code_bytes(2) == 4096 and kv.kvarn_tile_code_bytes(4) == 8192
     assert kv.kvarn_tile_code_bytes(3) == 0 and kv.kvarn_tile_param_bytes() == 512
-    for s in range(5):
+    for s in range(6):
         assert kv.kvarn_status_string(s).startswith("KVARN_")
+    assert "TIMEOUT" in kv.kvarn_status_string(5)
 
 
 def _cfg(**kw):
@@ -240,3 +241,11 @@ def test_append_validation_needs_no_gpu(lib):
     assert call(B=0) == 0
     assert lib.kvarn_append_workspace_size(2, 2) >= 2 * 4 * 32768
     assert lib.kvarn_append_workspace_size(0, 0) == 0
+
+
+def test_bounded_wait_check_validation_needs_no_gpu(lib):
+    # the self-check's limit is validated on the host; nothing is enqueued on error
+    assert lib.kvarn_check_bounded_wait(0, None) == 1
+    assert lib.kvarn_check_bounded_wait(1000001, None) == 1
+    assert b"limit_us" in lib.kvarn_last_error()
+    assert lib.kvarn_status_string(5) == b"KVARN_ERR_TIMEOUT: a bounded device wait gave up"
