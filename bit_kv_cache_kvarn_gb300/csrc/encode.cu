@@ -42,6 +42,7 @@ struct EncodeSmem {
         float ys[kTile * kYStride];        // FWHT staging (72 KB), dead after the second pass
         struct {
             float2 red[kWarps][4][32];     // cross-warp partial sums (8 KB)
+            float cmean[kTile];            // channel means: the shift of a second channel pass
             alignas(16) uint32_t codes[kTile * 16];  // packed rows (up to 8 KB)
         } late;
     } u;
@@ -178,72 +179,68 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
     // token step:   r_t = std_j(Y_tj / c_j)   (lane owns token kown of its 8 for the update)
     // channel step: c_j = std_t(Y_tj / r_t)
     // The factors are kept as their inverses b = 1/r, a = 1/c (one rsqrt each).
+    // Each step sums p and p^2 (p = Y a, resp. Y b) and takes var = E[p^2] - E[p]^2.  In fp32 that
+    // loses ~log2(ms / var) bits to cancellation when a row or column is dominated by its mean (K
+    // with a large per-channel bias, V with a per-token offset after the rotation moves it into one
+    // channel); so a step in which some row (column) has var < ms / 8 is summed again over
+    // d = p - mean, with the mean just found as the shift: E[d^2] - E[d]^2 has no cancellation.
+    // Ordinary tiles never take that second pass (the first pass alone is exact to ~1e-7 there).
+    constexpr float kRedo = 0.125f;
     float b_own = 1.f;
     float2 a2[4];  // (a, a) of channels h + 16 (2 m), h + 16 (2 m + 1)
 #pragma unroll
     for (int m = 0; m < 4; ++m) a2[m] = make_float2(1.f, 1.f);
     if (tid < kTile) sm.cinv[tid] = 1.f;
-    const int n_it = normalize ? iters : 0;
-    for (int itn = 0; itn < n_it; ++itn) {
-        // token step: acc[k] = (sum_j Y a, sum_j (Y a)^2) over this thread's channels
+    // lane holding the statistics of this thread's token slot k (k ^ kown is that lane's kown)
+    auto slot_src = [&](int k) {
+        const int kt = k ^ kown;
+        return (lane & 16) | (((kt >> 2) & 1) << 3) | (((kt >> 1) & 1) << 2) | ((kt & 1) << 1);
+    };
+    // token step sums (sum d, sum d^2), d = Y a + sh, over the 128 channels of this lane's token
+    // kown: thread partials, then a transposing reduction over the 16 channel lanes
+    auto token_sums = [&](auto shifted, const float2 (&sh)[8]) -> float2 {
         float2 acc[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            float2 p = fmul2(y[k][0], a2[0]);
+            float2 p = decltype(shifted)::value ? ffma2(y[k][0], a2[0], sh[k]) : fmul2(y[k][0], a2[0]);
             float2 s1 = p, s2 = fmul2(p, p);
 #pragma unroll
             for (int m = 1; m < 4; ++m) {
-                p = fmul2(y[k][m], a2[m]);
+                p = decltype(shifted)::value ? ffma2(y[k][m], a2[m], sh[k]) : fmul2(y[k][m], a2[m]);
                 s1 = fadd2(s1, p);
                 s2 = ffma2(p, p, s2);
             }
             acc[k] = make_float2(s1.x + s1.y, s2.x + s2.y);
         }
-        // transposing reduction over the 16 channel lanes
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float2 send = acc[q + 4];
-            float2 keep = acc[q];
-            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 8),
-                                                   __shfl_xor_sync(0xffffffffu, send.y, 8)));
-            acc[q] = keep;
+            acc[q] = fadd2(acc[q], make_float2(__shfl_xor_sync(0xffffffffu, send.x, 8),
+                                               __shfl_xor_sync(0xffffffffu, send.y, 8)));
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const float2 send = acc[q + 2];
-            float2 keep = acc[q];
-            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
-                                                   __shfl_xor_sync(0xffffffffu, send.y, 4)));
-            acc[q] = keep;
+            acc[q] = fadd2(acc[q], make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
+                                               __shfl_xor_sync(0xffffffffu, send.y, 4)));
         }
-        {
-            const float2 send = acc[1];
-            float2 keep = acc[0];
-            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 2),
-                                                   __shfl_xor_sync(0xffffffffu, send.y, 2)));
-            keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, keep.x, 1),
-                                                   __shfl_xor_sync(0xffffffffu, keep.y, 1)));
-            const float mean = keep.x * (1.f / kTile);
-            const float ms = keep.y * (1.f / kTile);
-            const float var = ms - mean * mean;
-            if (var > kDegenerateRel * ms) b_own = rsqrtf(var);
-        }
-        float2 bb[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int kt = k ^ kown;  // the lane owning slot k's token has kown == kt
-            const int src = (lane & 16) | (((kt >> 2) & 1) << 3) | (((kt >> 1) & 1) << 2) | ((kt & 1) << 1);
-            const float b = __shfl_sync(0xffffffffu, b_own, src);
-            bb[k] = make_float2(b, b);
-        }
-        // channel step: acc[i] = (sum_t Y b, sum_t (Y b)^2) for channel h + 16 i
+        float2 keep = fadd2(acc[0], make_float2(__shfl_xor_sync(0xffffffffu, acc[1].x, 2),
+                                                __shfl_xor_sync(0xffffffffu, acc[1].y, 2)));
+        return fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, keep.x, 1),
+                                       __shfl_xor_sync(0xffffffffu, keep.y, 1)));
+    };
+    // channel step partial sums (sum d, sum d^2), d = Y b + csh, of this thread's 8 tokens for its
+    // 8 channels, combined over the half-warp pair into the cross-warp scratch
+    float2 bb[8];
+    auto channel_sums = [&](auto shifted, const float2 (&csh)[4]) {
+        float2 acc[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            float2 p = fmul2(y[0][m], bb[0]);
+            float2 p = decltype(shifted)::value ? ffma2(y[0][m], bb[0], csh[m]) : fmul2(y[0][m], bb[0]);
             float2 s1 = p, s2 = fmul2(p, p);
 #pragma unroll
             for (int k = 1; k < 8; ++k) {
-                p = fmul2(y[k][m], bb[k]);
+                p = decltype(shifted)::value ? ffma2(y[k][m], bb[k], csh[m]) : fmul2(y[k][m], bb[k]);
                 s1 = fadd2(s1, p);
                 s2 = ffma2(p, p, s2);
             }
@@ -255,26 +252,74 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
             float2 send = tsub ? acc[q] : acc[q + 4];
             float2 keep = tsub ? acc[q + 4] : acc[q];
             keep = fadd2(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 16),
-                                                   __shfl_xor_sync(0xffffffffu, send.y, 16)));
+                                           __shfl_xor_sync(0xffffffffu, send.y, 16)));
             sm.u.late.red[warp][q][lane] = keep;  // channel h + 16 (q + 4 tsub)
         }
-        __syncthreads();
-        if (tid < kTile) {
-            const int j = tid, hj = j & 15, ij = j >> 4;
-            const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
-            float2 s = make_float2(0.f, 0.f);
+    };
+    // channel tid's total over the 8 warps (threads 0..127)
+    auto channel_total = [&]() -> float2 {
+        const int hj = tid & 15, ij = tid >> 4;
+        const int src_lane = ((ij >> 2) << 4) | hj, q = ij & 3;
+        float2 s = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                s = fadd2(s, sm.u.late.red[w][q][src_lane]);
+        for (int w = 0; w < kWarps; ++w) s = fadd2(s, sm.u.late.red[w][q][src_lane]);
+        return s;
+    };
+    const float2 no_shift8[8] = {};
+    const float2 no_shift4[4] = {};
+    const int n_it = normalize ? iters : 0;
+    for (int itn = 0; itn < n_it; ++itn) {
+        {
+            const float2 t1 = token_sums(std::false_type(), no_shift8);
+            const float mean = t1.x * (1.f / kTile);
+            const float ms = t1.y * (1.f / kTile);
+            float var = ms - mean * mean;
+            if (__any_sync(0xffffffffu, var < kRedo * ms)) {  // warp-uniform
+                float2 sh[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float mk = __shfl_sync(0xffffffffu, mean, slot_src(k));
+                    sh[k] = make_float2(-mk, -mk);
+                }
+                const float2 t2 = token_sums(std::true_type(), sh);
+                const float dm = t2.x * (1.f / kTile);
+                var = t2.y * (1.f / kTile) - dm * dm;
             }
-            const float mean = s.x * (1.f / kTile);
-            const float ms = s.y * (1.f / kTile);
-            const float var = ms - mean * mean;
-            float a = sm.cinv[j];
-            if (var > kDegenerateRel * ms) a = rsqrtf(var);
-            sm.cinv[j] = a;
+            if (var > kDegenerateRel * ms) b_own = rsqrtf(var);
         }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float b = __shfl_sync(0xffffffffu, b_own, slot_src(k));
+            bb[k] = make_float2(b, b);
+        }
+        channel_sums(std::false_type(), no_shift4);
         __syncthreads();
+        float cms = 0.f;
+        bool redo = false;
+        if (tid < kTile) {
+            const float2 s = channel_total();
+            const float mean = s.x * (1.f / kTile);
+            cms = s.y * (1.f / kTile);
+            const float var = cms - mean * mean;
+            redo = var < kRedo * cms;
+            sm.u.late.cmean[tid] = mean;  // the shift of a second pass
+            if (!redo && var > kDegenerateRel * cms) sm.cinv[tid] = rsqrtf(var);
+        }
+        if (__syncthreads_or(redo)) {  // block-uniform: some column is dominated by its mean
+            float2 csh[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                csh[m] = make_float2(-sm.u.late.cmean[h + 32 * m], -sm.u.late.cmean[h + 32 * m + 16]);
+            channel_sums(std::true_type(), csh);
+            __syncthreads();
+            if (tid < kTile) {
+                const float2 s = channel_total();
+                const float dm = s.x * (1.f / kTile);
+                const float var = s.y * (1.f / kTile) - dm * dm;
+                if (var > kDegenerateRel * cms) sm.cinv[tid] = rsqrtf(var);
+            }
+            __syncthreads();
+        }
 #pragma unroll
         for (int m = 0; m < 4; ++m) a2[m] = make_float2(sm.cinv[h + 32 * m], sm.cinv[h + 32 * m + 16]);
     }

@@ -119,7 +119,7 @@ def fp16_round(x: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------------------------
 # Dual-axis variance normalisation
 # ----------------------------------------------------------------------------------------------
-def dual_axis_normalize(y: np.ndarray, iters: int = DEFAULT_ITERS):
+def dual_axis_normalize(y: np.ndarray, iters: int = DEFAULT_ITERS, trace: list | None = None):
     """Sinkhorn-Knopp style alternating standard-deviation normalisation in the log domain.
 
     Returns (log_r, log_c): log token factors (one per row) and log channel factors (one per
@@ -136,22 +136,30 @@ def dual_axis_normalize(y: np.ndarray, iters: int = DEFAULT_ITERS):
       * factors start at 1 and each step adds log(sigma) of the currently normalised matrix;
       * a row/column whose variance is <= DEGENERATE_REL times its mean square (including an
         all-zero one) is treated as constant: its factor is left unchanged.
+    trace: optional list; each step appends ("token" | "channel", iteration, var / ms) so a test can
+    see how far each row's or column's degeneracy decision is from the threshold.
     """
     y = np.asarray(y, dtype=np.float64)
     log_r = np.zeros(y.shape[0])
     log_c = np.zeros(y.shape[1])
-    for _ in range(iters):
+    for it in range(iters):
         # token step: each row's std over channels
         z = y / np.exp(log_r)[:, None] / np.exp(log_c)[None, :]
         var = z.var(axis=1)
         ms = (z * z).mean(axis=1)
         ok = var > DEGENERATE_REL * ms
+        if trace is not None:
+            with np.errstate(divide="ignore", invalid="ignore"):
+                trace.append(("token", it, var / ms))
         log_r[ok] += 0.5 * np.log(var[ok])
         # channel step: each column's std over tokens
         z = y / np.exp(log_r)[:, None] / np.exp(log_c)[None, :]
         var = z.var(axis=0)
         ms = (z * z).mean(axis=0)
         ok = var > DEGENERATE_REL * ms
+        if trace is not None:
+            with np.errstate(divide="ignore", invalid="ignore"):
+                trace.append(("channel", it, var / ms))
         log_c[ok] += 0.5 * np.log(var[ok])
     return log_r, log_c
 

@@ -44,14 +44,33 @@ def test_config0_tiny_codec(kv):
     _check(kv, cfg, v.reshape(8, 128, 128).cuda(), "config0")
 
 
-@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+ALL_PRESETS = ["kvarn_k4v2_g128", "kvarn_k2v2_g128", "kvarn_k4v4_g128", "kvarn_k2v4_g128"]
+
+
+@pytest.mark.parametrize("preset", ALL_PRESETS)
 def test_config1_batched_encode_full(kv, preset):
-    # 64 sequences x 8 kv heads x one 128-token block, seed 1: 512 K tiles and 512 V tiles
+    # 64 sequences x 8 kv heads x one 128-token block, seed 1: 512 K tiles and 512 V tiles through
+    # the fused K+V call, every tile against the oracle (including the 4-bit V encoder of the K4/V4
+    # and K2/V4 presets); the single-kind calls must give the same bytes
     k, v = kv.synthetic.outlier_kv(1, 64 * 8, 128, device="cuda")
+    k, v = k.reshape(-1, 128, 128), v.reshape(-1, 128, 128)
+    n = k.shape[0]
     cfg = kv.kvarn_config_from_preset(preset)
-    res_k = _check(kv, cfg, k.reshape(-1, 128, 128), preset + " K-cache", kinds=("K",))
-    res_v = _check(kv, cfg, v.reshape(-1, 128, 128), preset + " V-cache", kinds=("V",))
-    for st in (res_k["K"][3], res_v["V"][3]):
+    outs = []
+    for bits in (cfg.k_bits, cfg.v_bits):
+        outs += [torch.full((n, 128 * 16 * bits), 7, dtype=torch.uint8, device="cuda"),
+                 torch.full((n, 512), 7, dtype=torch.uint8, device="cuda"),
+                 torch.full((n,), 7.0, dtype=torch.float32, device="cuda")]
+    kv.kvarn_encode_kv_blocks(cfg, k, v, *outs)
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_error() == 0
+    sep = list(_encode_gpu(kv, cfg, kv.KVARN_KIND_K, k)) + list(_encode_gpu(kv, cfg, kv.KVARN_KIND_V, v))
+    for got, want in zip(outs, sep):
+        assert torch.equal(got, want)
+    for name, x, (c, p_, sc), bits in (("K", k, outs[:3], cfg.k_bits), ("V", v, outs[3:], cfg.v_bits)):
+        st = compare_encode(x.float().cpu().double().numpy(), name, bits, c.cpu().numpy(), p_.cpu().numpy(),
+                            sc.cpu().numpy())
+        print(preset, name, st)
         assert st["free_code_mismatch"] <= 1e-4 * st["elements"]
 
 
@@ -94,7 +113,7 @@ def test_persistent_grid_many_tiles_and_empty(kv):
                            empty, empty, torch.empty(0, device="cuda"))
 
 
-@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+@pytest.mark.parametrize("preset", ALL_PRESETS)
 @pytest.mark.parametrize("n", [512, 77, 1])
 def test_fused_kv_encode_equals_separate_calls(kv, preset, n):
     # one launch over K and V tiles gives the two single-kind results bit for bit; the first
@@ -117,7 +136,7 @@ def test_fused_kv_encode_equals_separate_calls(kv, preset, n):
                        res[1][:m].cpu().numpy(), res[2][:m].cpu().numpy())
 
 
-@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v2_g128"])
+@pytest.mark.parametrize("preset", ALL_PRESETS)
 def test_dequant_matches_oracle_on_identical_packed_input(kv, preset):
     cfg = kv.kvarn_config_from_preset(preset)
     k, v = kv.synthetic.outlier_kv(8, 40, 128, device="cuda")
@@ -137,3 +156,44 @@ def test_dequant_matches_oracle_on_identical_packed_input(kv, preset):
                 assert np.abs(got[t] - ref[t]).max() <= 1e-3 * rms
         # reconstruction quality sanity: the codec estimate is close to the input
         assert rel_l2(got, x.float().cpu().double().numpy()) < (0.5 if bits == 2 else 0.15)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128", "kvarn_k2v4_g128"])
+def test_mean_dominated_tiles(kv, preset, flags):
+    # K with a per-channel bias of 30x, 100x and 300x its within-channel std, V with per-token
+    # offsets of the same sizes: rows or columns whose variance is a small fraction of their mean
+    # square, where a one-pass fp32 variance would lose most of its digits; with and without the
+    # rotation (without it the biases reach the normalisation unrotated)
+    from tests import _tiles
+
+    base = kv.kvarn_config_from_preset(preset)
+    cfg = kv.make_config(base.k_bits, base.v_bits, 8, flags)
+    xk = _tiles.biased_k_tiles(61).cuda()
+    xv = _tiles.offset_v_tiles(62).cuda()
+    _check(kv, cfg, xk, f"biased K flags={flags}", rotate=not flags, kinds=("K",))
+    _check(kv, cfg, xv, f"offset V flags={flags}", rotate=not flags, kinds=("V",))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_degeneracy_threshold_rows_and_columns(kv, bits):
+    # rows (and, in a second tile, columns) whose variance is 0.56x, 0.985x, 1.012x and 2.07x of
+    # 1e-5 times their mean square when the normalisation first meets them: the ones below keep
+    # their factor, the ones above are normalised, and the kernel must decide each as the oracle
+    # does (no rotation, so the constructed rows reach the normalisation unchanged)
+    from tests import _tiles
+
+    cfg = kv.make_config(bits, bits, 8, 1)
+    xr, rows = _tiles.threshold_row_tile(1)
+    xc, cols = _tiles.threshold_column_tile(2)
+    for x, where, axis in ((xr, rows, "token"), (xc, cols, "channel")):
+        # precondition: the constructed rows / columns sit at their ratios, and no decision the
+        # oracle takes on the tile is within 0.5% of the threshold
+        trace = []
+        o.dual_axis_normalize(x.float().double().numpy(), 8, trace=trace)
+        first = trace[0 if axis == "token" else 1][2]
+        for label, i in where.items():
+            want = float(label[:-1])
+            assert abs(first[i] / 1e-5 / want - 1) < 0.03, (axis, label, first[i])
+        assert min(np.nanmin(np.abs(r[2] / 1e-5 - 1)) for r in trace) > 5e-3
+        _check(kv, cfg, x[None].cuda(), f"threshold {axis}s", rotate=False)

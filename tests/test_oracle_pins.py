@@ -144,6 +144,25 @@ def test_normalization_degenerate_rows_and_columns_keep_factor():
     assert np.all(np.isfinite(log_r)) and np.all(np.isfinite(log_c))
 
 
+def test_normalization_threshold_of_near_constant_rows_closed_form():
+    # A row of two levels c and c + 1 with k of 128 entries at c + 1 has, in closed form,
+    # variance f (1 - f) and mean square (c + f)^2 + f (1 - f), f = k / 128.  In the first token
+    # step (all channel factors 1) the row's factor is its std when var / ms > 1e-5, else it stays 1
+    # -- rows at 0.56x, 0.985x, 1.012x and 2.07x of the threshold land on the predicted sides.
+    from tests import _tiles
+
+    x, rows = _tiles.threshold_row_tile(1)
+    y = x.float().double().numpy()
+    log_r, _ = o.dual_axis_normalize(y, 1)
+    for label, t in rows.items():
+        c, k = _tiles.THRESHOLD_LEVELS[label]
+        f = k / 128
+        var, ms = f * (1 - f), (c + f) ** 2 + f * (1 - f)
+        want = 0.5 * np.log(var) if var > 1e-5 * ms else 0.0
+        assert (var > 1e-5 * ms) == (label in ("1.012x", "2.07x"))
+        assert abs(log_r[t] - want) <= 1e-12, label
+
+
 # --- encode -----------------------------------------------------------------------------------
 @pytest.mark.parametrize("kind", ["K", "V"])
 @pytest.mark.parametrize("bits", [2, 4])
