@@ -22,29 +22,22 @@ import time
 
 import torch
 
+from . import synthetic
+
 HEAD = 128
 BLOCK = 128
 ROPE_BASE = 1e6
 RMS_EPS = 1e-6
 
 
-def make_weights(seed: int, layers: int, hidden: int, hq: int, hkv: int, device="cuda"):
-    """Per layer {wq [hq*128, D], wk, wv [hkv*128, D], wo [D, hq*128]}, N(0, 0.02), bf16."""
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    out = []
-    for _ in range(layers):
-        w = {}
-        for name, shape in (("wq", (hq * HEAD, hidden)), ("wk", (hkv * HEAD, hidden)),
-                            ("wv", (hkv * HEAD, hidden)), ("wo", (hidden, hq * HEAD))):
-            w[name] = (torch.randn(shape, generator=g) * 0.02).to(torch.bfloat16).to(device)
-        out.append(w)
-    return out
+def make_weights(seed: int, layers: int, hidden: int, hq: int, hkv: int, device="cuda", kv_outliers=False):
+    """The stack's weights (synthetic.pseudo_decode_weights) on `device`."""
+    return synthetic.pseudo_decode_weights(seed, layers, hidden, hq, hkv, device, kv_outliers)
 
 
 def make_input(seed: int, tokens: int, hidden: int, device="cuda"):
-    """Layer-0 inputs [tokens, hidden], N(0, 1), bf16."""
-    g = torch.Generator(device="cpu").manual_seed(seed + 7919)
-    return torch.randn(tokens, hidden, generator=g).to(torch.bfloat16).to(device)
+    """Layer-0 inputs [tokens, hidden] (synthetic.pseudo_decode_input) on `device`."""
+    return synthetic.pseudo_decode_input(seed, tokens, hidden, device)
 
 
 def _rmsnorm(x):
@@ -75,9 +68,12 @@ def _exact_attention(q, k_all, v_all, n_prev, scale):
     return torch.bmm(torch.softmax(s, dim=-1), vv).permute(1, 0, 2)  # [T, Hq, 128]
 
 
-def run(kv, cfg, weights, x, hq: int, hkv: int, quantised: bool = True, capture=None):
+def run(kv, cfg, weights, x, hq: int, hkv: int, quantised: bool = True, capture=None, kv_token_scale=None):
     """Free-running pseudo-decode over all blocks of x.  Returns (attn, seconds) with attn[j][l]
     the fp32 attention output [128, hq, 128] of block j, layer l.
+
+    kv_token_scale: optional [tokens] multipliers of each position's K and V projections (the
+    outlier variant, synthetic.pseudo_decode_token_scales).
 
     capture: optional dict keyed by (block, layer); for each key present the codec's inputs and
     output at that point are stored as its value -- dict(q, k_blk, v_blk, attn, pools,
@@ -115,6 +111,7 @@ def run(kv, cfg, weights, x, hq: int, hkv: int, quantised: bool = True, capture=
     if quantised:
         ws = torch.empty(kv.kvarn_decode_workspace_size(cfg_dec, BLOCK, hq, hkv, max_tiles) // 4 + 4, device=dev)
     out = torch.empty(BLOCK, hq, HEAD, device=dev)
+    tok_scale = None if kv_token_scale is None else kv_token_scale.to(device=dev, dtype=torch.float32)
     attn = []
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -125,8 +122,13 @@ def run(kv, cfg, weights, x, hq: int, hkv: int, quantised: bool = True, capture=
         for l, w in enumerate(weights):
             n = _rmsnorm(h)
             q = _rope((n @ w["wq"].float().T).reshape(BLOCK, hq, HEAD), pos).to(torch.bfloat16)
-            k = _rope((n @ w["wk"].float().T).reshape(BLOCK, hkv, HEAD), pos).to(torch.bfloat16)
-            v = (n @ w["wv"].float().T).reshape(BLOCK, hkv, HEAD).to(torch.bfloat16)
+            k_proj = n @ w["wk"].float().T
+            v_proj = n @ w["wv"].float().T
+            if tok_scale is not None:
+                ts = tok_scale[j * BLOCK:(j + 1) * BLOCK, None]
+                k_proj, v_proj = k_proj * ts, v_proj * ts
+            k = _rope(k_proj.reshape(BLOCK, hkv, HEAD), pos).to(torch.bfloat16)
+            v = v_proj.reshape(BLOCK, hkv, HEAD).to(torch.bfloat16)
             if quantised:
                 kc, kp, ks, vc, vp, vs = pools[l]
                 lens = (j * BLOCK + 1 + torch.arange(BLOCK, device=dev, dtype=torch.int32)).contiguous()
@@ -165,9 +167,19 @@ def mae_curves(attn_q, attn_ref, relative: bool = False):
             for rq, rr in zip(attn_q, attn_ref)]
 
 
+def presets(kv):
+    """The codecs the MAE curves compare: KVarN (2-bit and 4-bit K), rotation only, plain RTN."""
+    return (("kvarn_k2v2", kv.kvarn_config_from_preset("kvarn_k2v2_g128")),
+            ("kvarn_k4v2", kv.kvarn_config_from_preset("kvarn_k4v2_g128")),
+            ("hadamard_k2v2 (rotation, no normalisation)", kv.kvarn_config_from_preset("hadamard_k2v2_g128")),
+            ("rtn_k2v2 (no rotation, no normalisation)", kv.kvarn_config_from_preset("kivi_k2v2_g128")))
+
+
 def main():
     """Config 4 (4 layers, 32q/8kv, hidden 4096, 64 blocks of 128 tokens, seed 4): MAE per block
-    and layer of the KVarN cache and of the same stack with rotation and normalisation off."""
+    and layer of each codec's cache against the unquantised run.  --kv-outliers runs the variant
+    whose K/V carry the outlier structure of the cache recipe (synthetic.pseudo_decode_weights,
+    synthetic.pseudo_decode_token_scales)."""
     import argparse
     import json
 
@@ -180,19 +192,19 @@ def main():
     ap.add_argument("--hkv", type=int, default=8)
     ap.add_argument("--blocks", type=int, default=64)
     ap.add_argument("--seed", type=int, default=4)
+    ap.add_argument("--kv-outliers", action="store_true")
     args = ap.parse_args()
     kv.load()
-    w = make_weights(args.seed, args.layers, args.hidden, args.hq, args.hkv)
+    w = make_weights(args.seed, args.layers, args.hidden, args.hq, args.hkv, kv_outliers=args.kv_outliers)
     x = make_input(args.seed, args.blocks * BLOCK, args.hidden)
-    cfg = kv.kvarn_config_from_preset("kvarn_k2v2_g128")
-    ref, t_ref = run(kv, None, w, x, args.hq, args.hkv, quantised=False)
+    ts = synthetic.pseudo_decode_token_scales(args.seed, args.blocks * BLOCK) if args.kv_outliers else None
+    ref, t_ref = run(kv, None, w, x, args.hq, args.hkv, quantised=False, kv_token_scale=ts)
     res = {"config": vars(args), "reference_s": round(t_ref, 3)}
-    for name, c in (("kvarn_k2v2", cfg), ("kvarn_k4v2", kv.kvarn_config_from_preset("kvarn_k4v2_g128")),
-                    ("rtn_k2v2 (no rotation, no normalisation)", kv.make_config(k_bits=2, v_bits=2, sinkhorn_iters=0,
-                                                                                flags=3))):
-        a, t = run(kv, c, w, x, args.hq, args.hkv, quantised=True)
+    for name, c in presets(kv):
+        a, t = run(kv, c, w, x, args.hq, args.hkv, quantised=True, kv_token_scale=ts)
         res[name] = {"seconds": round(t, 3), "mae": mae_curves(a, ref),
                      "relative_mae": mae_curves(a, ref, relative=True)}
+    assert kv.kvarn_device_error() == 0
     print(json.dumps(res))
 
 

@@ -64,3 +64,51 @@ def tile_permutation(seed: int, n: int, device="cpu") -> torch.Tensor:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed + 3_000_003)
     return torch.randperm(n, generator=gen).to(device)
+
+
+# ---- the block pseudo-decode stack (an attention-only model with random weights) --------------
+def pseudo_decode_weights(seed: int, layers: int, hidden: int, hq: int, hkv: int, device="cpu",
+                          kv_outliers: bool = False):
+    """Per layer {wq [hq*128, D], wk, wv [hkv*128, D], wo [D, hq*128]}, N(0, 0.02), bf16.
+
+    kv_outliers: give the K and V projections the outlier channels of the cache recipe above --
+    each output row (one channel of one kv head) of W_K, and separately of W_V, is multiplied by
+    lognormal(0, 1), and 4 distinct channels per kv head by a further x20 -- drawn from a second
+    generator, so the base weights are the same with and without."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    out = []
+    for _ in range(layers):
+        w = {}
+        for name, shape in (("wq", (hq * HEAD_DIM, hidden)), ("wk", (hkv * HEAD_DIM, hidden)),
+                            ("wv", (hkv * HEAD_DIM, hidden)), ("wo", (hidden, hq * HEAD_DIM))):
+            w[name] = torch.randn(shape, generator=g) * 0.02
+        out.append(w)
+    if kv_outliers:
+        g2 = torch.Generator(device="cpu").manual_seed(seed + 104_729)
+        for w in out:
+            for name in ("wk", "wv"):
+                chan = torch.exp(torch.randn(hkv, HEAD_DIM, generator=g2))
+                pick = torch.rand(hkv, HEAD_DIM, generator=g2).argsort(dim=1)[:, :4]
+                chan.scatter_(1, pick, chan.gather(1, pick) * 20.0)
+                w[name] = w[name] * chan.reshape(-1, 1)
+    return [{k: v.to(torch.bfloat16).to(device) for k, v in w.items()} for w in out]
+
+
+def pseudo_decode_input(seed: int, tokens: int, hidden: int, device="cpu") -> torch.Tensor:
+    """Layer-0 inputs [tokens, hidden], N(0, 1), bf16."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 7919)
+    return torch.randn(tokens, hidden, generator=g).to(torch.bfloat16).to(device)
+
+
+def pseudo_decode_token_scales(seed: int, tokens: int) -> torch.Tensor:
+    """Per-position multipliers of the K and V projections for the outlier variant of the stack:
+    lognormal(0, 0.5), with round(5% of positions) distinct positions x8 -- the token part of the
+    cache recipe above.  (A pre-norm model removes any scale of its input tokens, so the variant
+    applies them to the projections' outputs.)  float32 [tokens] on the CPU."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 130_363)
+    tok = torch.exp(0.5 * torch.randn(tokens, generator=g))
+    n_out = int(round(0.05 * tokens))
+    if n_out > 0:
+        pick = torch.rand(tokens, generator=g).argsort()[:n_out]
+        tok[pick] *= 8.0
+    return tok

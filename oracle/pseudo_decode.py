@@ -96,9 +96,13 @@ def quantise_block(kv_blk: np.ndarray, kind: str, bits: int, iters: int, rotate:
 
 def run(weights, x, hq: int, hkv: int, quantised: bool, k_bits: int = 2, v_bits: int = 2,
         iters: int = o.DEFAULT_ITERS, rotate: bool = True, normalize: bool = True,
-        block: int = o.TILE):
+        block: int = o.TILE, kv_token_scale=None):
     """Free-running pseudo-decode.  weights: list of dicts with wq [Hq*128, D], wk, wv
-    [Hkv*128, D], wo [D, Hq*128]; x: [T, D] layer-0 inputs.  Returns attn[j][l]: [block, Hq, 128]."""
+    [Hkv*128, D], wo [D, Hq*128]; x: [T, D] layer-0 inputs.  Returns attn[j][l]: [block, Hq, 128].
+
+    kv_token_scale: optional [T] multipliers of each position's K and V projections, for a stack
+    whose K/V carry token-scale outliers (the pages' caches have them; a pre-norm stack would
+    remove any scale of its input tokens, so it is applied to the projections' outputs)."""
     x = np.asarray(x, dtype=np.float64)
     n_blocks = x.shape[0] // block
     scale = 1.0 / np.sqrt(HEAD)
@@ -111,8 +115,12 @@ def run(weights, x, hq: int, hkv: int, quantised: bool, k_bits: int = 2, v_bits:
         for l, w in enumerate(weights):
             n = rmsnorm(h)
             q = rope((n @ w["wq"].T).reshape(block, hq, HEAD), pos)
-            k = rope((n @ w["wk"].T).reshape(block, hkv, HEAD), pos)
-            v = (n @ w["wv"].T).reshape(block, hkv, HEAD)
+            kp, vp = n @ w["wk"].T, n @ w["wv"].T
+            if kv_token_scale is not None:
+                ts = np.asarray(kv_token_scale, dtype=np.float64)[j * block:(j + 1) * block, None]
+                kp, vp = kp * ts, vp * ts
+            k = rope(kp.reshape(block, hkv, HEAD), pos)
+            v = vp.reshape(block, hkv, HEAD)
             q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
             kc, vc = caches[l]
             k_prev = np.concatenate(kc, axis=0) if kc else np.zeros((0, hkv, HEAD))

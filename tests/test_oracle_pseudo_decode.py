@@ -99,3 +99,29 @@ def test_quantised_pseudo_decode_first_block_is_exact_and_error_appears_after():
     e = o.encode_tile(k[:, 1], "K", 2)
     want = o.dequant_tile(e["codes"], e["S1"], e["s2"], e["Z"], e["g"], "K", original_basis=True)
     assert np.array_equal(got[:, 1], want)
+
+
+def test_kv_token_scale_scales_the_keys_and_values_of_each_position():
+    # the outlier variant's per-position multipliers act on the K and V projections only: with
+    # them, the unquantised run equals ordinary causal attention (torch SDPA, fp64) over keys and
+    # values scaled row by row, while the queries are unscaled
+    w, x = _tiny_model(47, layers=1)
+    hq, hkv, T = 4, 2, x.shape[0]
+    ts = np.exp(np.random.default_rng(48).standard_normal(T))
+    a = pd.run(w, x, hq, hkv, quantised=False, kv_token_scale=ts)
+    wl, pos = w[0], np.arange(T)
+    n = pd.rmsnorm(x)
+    q = pd.bf16_round(pd.rope((n @ wl["wq"].T).reshape(T, hq, 128), pos))
+    k = pd.bf16_round(pd.rope((n @ wl["wk"].T * ts[:, None]).reshape(T, hkv, 128), pos))
+    v = pd.bf16_round((n @ wl["wv"].T * ts[:, None]).reshape(T, hkv, 128))
+    mask = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    for h in range(hq):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[:, h])[None], torch.from_numpy(k[:, h // 2])[None],
+            torch.from_numpy(v[:, h // 2])[None], attn_mask=mask[None], scale=1 / np.sqrt(128))[0].numpy()
+        for j in range(3):
+            assert np.abs(a[j][0][:, h] - ref[128 * j:128 * (j + 1)]).max() <= 1e-12
+    # all-ones multipliers are no multipliers
+    plain = pd.run(w, x, hq, hkv, quantised=False)
+    ones = pd.run(w, x, hq, hkv, quantised=False, kv_token_scale=np.ones(T))
+    assert all(np.array_equal(p_, o_) for rp, ro in zip(plain, ones) for p_, o_ in zip(rp, ro))
