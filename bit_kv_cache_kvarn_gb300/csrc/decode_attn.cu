@@ -508,7 +508,7 @@ decode_split_kernel(DecodeArgs a) {
     float* einv = qrs + GH * kTile;                        // [8]
     float* mpart = einv + 8;                               // [4 warps][8]
     float* lpart = mpart + 32;                             // [4 warps][8]
-    float* zkpart = lpart + 32;                            // [4 warps][8] partial sum_j q' Z_j
+    float* zkpart = lpart + 32;                            // sum_j q'_j Z_j: [head] (GH <= 4) or [4 warps][8]
     float* zvpart = zkpart + 32;                           // [4 warps][8] partial sum_t p Zv_t
     int* idring = reinterpret_cast<int*>(zvpart + 32);     // [kIdRing] tile ids (producer)
     uint8_t* cta = dsm + kWorkers * kWorkerStride;
@@ -710,20 +710,38 @@ decode_split_kernel(DecodeArgs a) {
                 load_row<KB>(sb + St::kK, r, x);
                 unpack_row_to_tmem<KB>(x, a_col + lane_off);
             }
-            {
+            if constexpr (GH <= 4) {
+                float xs[GH];
+                const float s1 = e4m3_value(sb[St::kKP + r]) * pre_k;
+#pragma unroll
+                for (int h = 0; h < GH; ++h) xs[h] = qreg[h] * s1;
+                store_b<GH>(bk, kk_k, xs);
+                // sum_j q'_j Z_j of head wq (one head per warp; lane l takes channels 4l..4l+3),
+                // read after the barrier below
+                if (wq < GH) {
+                    const float4 qv4 = *reinterpret_cast<const float4*>(qv + wq * kTile + 4 * lane);
+                    const uint2 zr = *reinterpret_cast<const uint2*>(sb + St::kKP + 256 + 8 * lane);
+                    const float2 z01 = __half22float2(*reinterpret_cast<const __half2*>(&zr.x));
+                    const float2 z23 = __half22float2(*reinterpret_cast<const __half2*>(&zr.y));
+                    float t = qv4.x * z01.x;
+                    t = fmaf(qv4.y, z01.y, t);
+                    t = fmaf(qv4.z, z23.x, t);
+                    t = fmaf(qv4.w, z23.y, t);
+                    t = warp_sum(t);
+                    if (lane == 0) zkpart[wq] = t;
+                }
+            } else {
                 float xs[GH], xz[GH];
                 const float s1 = e4m3_value(sb[St::kKP + r]) * pre_k;
                 const float z = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kKP + 256)[r]);
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    float q;
-                    if constexpr (kQReg) q = qreg[h];
-                    else q = qv[h * kTile + r];
+                    const float q = qv[h * kTile + r];
                     xs[h] = q * s1;
                     xz[h] = q * z;
                 }
                 store_b<GH>(bk, kk_k, xs);
-                // sum_j q'_j Z_j: per-warp partials, combined after the barrier below
+                // sum_j q'_j Z_j of eight heads: per-warp partials, combined after the barrier below
                 const float zsum = warp_sum_multi<GH>(xz, lane);
                 constexpr int kGroup = 32 / GH;
                 if ((lane & (kGroup - 1)) == 0) zkpart[wq * 8 + lane / kGroup] = zsum;
@@ -760,7 +778,12 @@ decode_split_kernel(DecodeArgs a) {
             float sc[GH], p[GH], zks[GH];
             const float tok = gk * e4m3_value(sb[St::kKP + 128 + r]);
             bool over = false;
-            sum_warp_parts<GH>(zkpart, zks);
+            if constexpr (GH <= 4) {
+#pragma unroll
+                for (int h = 0; h < GH; ++h) zks[h] = zkpart[h];
+            } else {
+                sum_warp_parts<GH>(zkpart, zks);
+            }
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
                 const float zk = zks[h];

@@ -94,13 +94,27 @@ __device__ __forceinline__ float tile_factor(float s_max, float m_max) {
     return e == INT_MIN ? 1.f : ldexpf(1.f, e);
 }
 
-// One tile in sm.xs (already arrived) -> codes, parameters and tile factor of output slot otile.
-// next: the tile this CTA encodes after it (its copy starts once sm.xs is consumed), or null.
-template <int BITS, int KIND>
-__device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16* next, uint8_t* __restrict__ codes_out,
-                                            uint8_t* __restrict__ params_out, float* __restrict__ scale_out,
-                                            int64_t otile, int iters, int rotate, int normalize) {
-    constexpr int kLevels = (1 << BITS) - 1;
+// Thread coordinates within the tile: the thread owns channels h + 16 i of tokens tg + 16 (k ^ kown).
+struct TileLanes {
+    int tid, lane, warp, h, tsub, tg, kown;
+    __device__ __forceinline__ TileLanes() {
+        tid = threadIdx.x;
+        lane = tid & 31;
+        warp = tid >> 5;
+        h = lane & 15;
+        tsub = lane >> 4;
+        tg = 2 * warp + tsub;
+        kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
+    }
+};
+
+// Stage 1 of a tile, the same for K and V: the tile in sm.xs (already arrived) is rotated into y
+// and normalised; on return the thread holds Y in y, the inverse token factor of its token kown in
+// b_own, and the inverse channel factors are in sm.cinv.  next: the tile this CTA encodes after it
+// (its copy starts once sm.xs is consumed), or null.
+__device__ __forceinline__ void rotate_normalise(EncodeSmem& sm, const TileLanes& L, const __nv_bfloat16* next,
+                                                 float2 (&y)[8][4], float& b_out, int iters, int rotate,
+                                                 int normalize) {
     constexpr uint32_t kTileBytes = kTile * kTile * 2;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -157,9 +171,8 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
     // as a 3-bit number: the partner lanes of the token reductions (h ^ 8, h ^ 4, h ^ 2) then
     // hold each other's tokens in complementary slots, so every lane keeps and sends the same
     // slots and no per-lane selection is needed; after the reduction lane h owns token kown.
-    const int kown = ((h >> 3) & 1) * 4 + ((h >> 2) & 1) * 2 + ((h >> 1) & 1);
+    const int kown = L.kown;
     // y[k][m]: token slot k, channels h + 16 (2 m) (.x) and h + 16 (2 m + 1) (.y)
-    float2 y[8][4];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int t = tg + 16 * (k ^ kown);
@@ -297,9 +310,9 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
         float cms = 0.f;
         bool redo = false;
         if (tid < kTile) {
-            const float2 s = channel_total();
-            const float mean = s.x * (1.f / kTile);
-            cms = s.y * (1.f / kTile);
+            const float2 t = channel_total();
+            const float mean = t.x * (1.f / kTile);
+            cms = t.y * (1.f / kTile);
             const float var = cms - mean * mean;
             redo = var < kRedo * cms;
             sm.u.late.cmean[tid] = mean;  // the shift of a second pass
@@ -313,9 +326,9 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
             channel_sums(std::true_type(), csh);
             __syncthreads();
             if (tid < kTile) {
-                const float2 s = channel_total();
-                const float dm = s.x * (1.f / kTile);
-                const float var = s.y * (1.f / kTile) - dm * dm;
+                const float2 t = channel_total();
+                const float dm = t.x * (1.f / kTile);
+                const float var = t.y * (1.f / kTile) - dm * dm;
                 if (var > kDegenerateRel * cms) sm.cinv[tid] = rsqrtf(var);
             }
             __syncthreads();
@@ -323,6 +336,19 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
 #pragma unroll
         for (int m = 0; m < 4; ++m) a2[m] = make_float2(sm.cinv[h + 32 * m], sm.cinv[h + 32 * m + 16]);
     }
+    b_out = b_own;
+}
+
+// Stage 2 of a tile, by kind: the scale split (s2, g, S1, Z), round-to-nearest codes, packing and the
+// stores to output slot otile.  y, b_own and sm.cinv as rotate_normalise leaves them.
+template <int BITS, int KIND>
+__device__ __forceinline__ void split_quantise_store(EncodeSmem& sm, const TileLanes& L, float2 (&y)[8][4],
+                                                     float b_own, uint8_t* __restrict__ codes_out,
+                                                     uint8_t* __restrict__ params_out,
+                                                     float* __restrict__ scale_out, int64_t otile, int rotate) {
+    constexpr int kLevels = (1 << BITS) - 1;
+    const int tid = L.tid, lane = L.lane, warp = L.warp, h = L.h, tsub = L.tsub, tg = L.tg, kown = L.kown;
+    (void)lane;
 
     // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
     // K: other axis = token (factor r); V: other axis = channel (factor c).
@@ -472,6 +498,14 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
         // on the wrong side, so near a half-way point the code is redone with a correctly
         // rounded division.  With the rotation the check is left out.
         constexpr float kRound = 12582912.f;
+        // With the rotation: v = sat(d / (S1 (2^b - 1))) in [0, 1] (one saturating multiply does
+        // both clamps) and r = v (2^b - 1) + kRound in one FFMA2, whose single rounding puts the
+        // nearest integer (half to even) of v (2^b - 1) in r's low bits.  The two roundings of
+        // 1 / (S1 (2^b - 1)) and of the product move u = (W / g - Z) / S1 by a few ulp, which
+        // changes a code only within a few ulp of a half-way point.
+        float is1l[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) is1l[m] = is1[m] * (1.f / (float)kLevels);
         auto quantise = [&](auto tie_check) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -480,14 +514,18 @@ __device__ __forceinline__ void encode_tile(EncodeSmem& sm, const __nv_bfloat16*
                     const int g0 = (KIND == KVARN_KIND_K) ? i : k, g1 = (KIND == KVARN_KIND_K) ? i + 1 : k;
                     const float2 d = ffma2(y[k][i >> 1], make_float2(inv_g, inv_g),
                                            make_float2(nz[g0], nz[g1]));
-                    const float2 u = fmul2(d, make_float2(is1[g0], is1[g1]));
+                    float2 rr;
+                    if (!decltype(tie_check)::value) {
+                        const float2 v = make_float2(mul_sat(d.x, is1l[g0]), mul_sat(d.y, is1l[g1]));
+                        rr = ffma2(v, make_float2((float)kLevels, (float)kLevels), make_float2(kRound, kRound));
+                    }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int ii = i + e, ge = e ? g1 : g0;
-                        const float ue = e ? u.y : u.x;
-                        float v = fminf(fmaxf(ue, 0.f), (float)kLevels);
-                        float r = v + kRound;
+                        float r = e ? rr.y : rr.x;
                         if (decltype(tie_check)::value) {
+                            float v = fminf(fmaxf((e ? d.y : d.x) * is1[ge], 0.f), (float)kLevels);
+                            r = v + kRound;
                             if (fabsf(v - (r - kRound)) > 0.4999f && is1[ge] > 0.f) {
                                 const int grp = (KIND == KVARN_KIND_K) ? (h + 16 * ii) : (tg + 16 * (k ^ kown));
                                 v = fminf(fmaxf(__fdiv_rn(e ? d.y : d.x, sm.grp_s1[pad(grp)]), 0.f), (float)kLevels);
@@ -574,12 +612,15 @@ encode_kernel(const __nv_bfloat16* __restrict__ x, int64_t n_tiles, uint8_t* __r
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& sm = *reinterpret_cast<EncodeSmem*>(smem_raw);
     encode_prologue(sm, blockIdx.x < n_tiles ? x + (int64_t)blockIdx.x * kTile * kTile : nullptr);
+    const TileLanes L;
     int local = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
         if (!encode_wait(sm, local)) break;
         const int64_t nt = tile + gridDim.x;
-        encode_tile<BITS, KIND>(sm, nt < n_tiles ? x + nt * kTile * kTile : nullptr, codes_out, params_out,
-                                scale_out, tile, iters, rotate, normalize);
+        float2 y[8][4];
+        float b_own;
+        rotate_normalise(sm, L, nt < n_tiles ? x + nt * kTile * kTile : nullptr, y, b_own, iters, rotate, normalize);
+        split_quantise_store<BITS, KIND>(sm, L, y, b_own, codes_out, params_out, scale_out, tile, rotate);
     }
 }
 
@@ -619,18 +660,21 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kv_kernel(EncodeKV a) {
     const int64_t n = a.n_k + a.n_v;
     int64_t tile = kv_next(a, blockIdx.x, n);
     encode_prologue(sm, tile < n ? kv_src(a, tile) : nullptr);
+    const TileLanes L;
     for (int local = 0; tile < n; ++local) {
         if (!encode_wait(sm, local)) break;
         const int64_t nt = kv_next(a, tile + gridDim.x, n);
         const __nv_bfloat16* next = nt < n ? kv_src(a, nt) : nullptr;
         const int64_t u = tile < a.n_k ? tile : tile - a.n_k;
         const int64_t slot = a.dest != nullptr ? (int64_t)a.dest[u] : u;
+        // the rotation and the normalisation are the same for both kinds: their code appears once
+        float2 y[8][4];
+        float b_own;
+        rotate_normalise(sm, L, next, y, b_own, a.iters, a.rotate, a.normalize);
         if (tile < a.n_k)
-            encode_tile<KB, KVARN_KIND_K>(sm, next, a.k_codes, a.k_params, a.k_scale, slot, a.iters, a.rotate,
-                                          a.normalize);
+            split_quantise_store<KB, KVARN_KIND_K>(sm, L, y, b_own, a.k_codes, a.k_params, a.k_scale, slot, a.rotate);
         else
-            encode_tile<VB, KVARN_KIND_V>(sm, next, a.v_codes, a.v_params, a.v_scale, slot, a.iters,
-                                          a.rotate, a.normalize);
+            split_quantise_store<VB, KVARN_KIND_V>(sm, L, y, b_own, a.v_codes, a.v_params, a.v_scale, slot, a.rotate);
         tile = nt;
     }
 }

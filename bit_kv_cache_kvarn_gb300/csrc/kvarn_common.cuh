@@ -26,6 +26,12 @@ constexpr long long kSpinLimit = 1ll << 24;      // try_wait polls before giving
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// a * b rounded to nearest and clamped to [0, 1] (one instruction)
+__device__ __forceinline__ float mul_sat(float a, float b) {
+    float r;
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 
 // ---- number formats (hardware conversions) ----------------------------------------------------
 __device__ __forceinline__ uint8_t e4m3_rn(float x) {
@@ -93,9 +99,24 @@ __device__ __forceinline__ uint64_t global_ns() {
 // (or kSpinLimit polls), sets *err_word and returns false; once *err_word is set by any thread of
 // the grid, every later wait returns false at once, so a stuck kernel ends within about a second.
 constexpr uint64_t kWaitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+constexpr int kFastPolls = 32;  // polls before the error word and the clock are consulted
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* err_word,
                                               uint64_t limit_ns) {
     const uint32_t addr = smem_addr(bar);
+    // Most waits end within a few polls (a tensor-core step, a copy issued long before); the first
+    // polls touch nothing but the barrier, so the error word's global load stays off that path.
+#pragma unroll 1
+    for (int f = 0; f < kFastPolls; ++f)
+        if (mbar_try_wait(addr, parity)) return true;
     uint64_t t0 = 0;
     for (long long i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
