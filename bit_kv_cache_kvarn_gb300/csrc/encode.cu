@@ -147,15 +147,13 @@ __device__ __forceinline__ void rotate_normalise(EncodeSmem& sm, const TileLanes
         if (rotate) fwht_pairs<8>(f);
         float* dst = sm.u.ys + t * kYStride + 16 * c;
         {
-            // 16-byte chunks stored in a lane-dependent rotation (bank-conflict free)
-            const int rot = (c >> 1) & 3;
-            float4 a0 = make_float4(f[0].x, f[0].y, f[1].x, f[1].y), a1 = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
-            float4 a2 = make_float4(f[4].x, f[4].y, f[5].x, f[5].y), a3 = make_float4(f[6].x, f[6].y, f[7].x, f[7].y);
-            rotl4(a0, a1, a2, a3, rot);
-            *reinterpret_cast<float4*>(dst + 4 * ((0 + rot) & 3)) = a0;
-            *reinterpret_cast<float4*>(dst + 4 * ((1 + rot) & 3)) = a1;
-            *reinterpret_cast<float4*>(dst + 4 * ((2 + rot) & 3)) = a2;
-            *reinterpret_cast<float4*>(dst + 4 * ((3 + rot) & 3)) = a3;
+            // 16-byte chunk q (channels 16 c + 4 q .. + 3) goes to position q ^ ((c >> 1) & 3) of the
+            // row's 16-channel group: the XOR spreads one store instruction's lanes over all banks
+            const int swz = (c >> 1) & 3;
+            *reinterpret_cast<float4*>(dst + 4 * (0 ^ swz)) = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+            *reinterpret_cast<float4*>(dst + 4 * (1 ^ swz)) = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+            *reinterpret_cast<float4*>(dst + 4 * (2 ^ swz)) = make_float4(f[4].x, f[4].y, f[5].x, f[5].y);
+            *reinterpret_cast<float4*>(dst + 4 * (3 ^ swz)) = make_float4(f[6].x, f[6].y, f[7].x, f[7].y);
         }
     }
     __syncthreads();
@@ -172,13 +170,18 @@ __device__ __forceinline__ void rotate_normalise(EncodeSmem& sm, const TileLanes
     // hold each other's tokens in complementary slots, so every lane keeps and sends the same
     // slots and no per-lane selection is needed; after the reduction lane h owns token kown.
     const int kown = L.kown;
-    // y[k][m]: token slot k, channels h + 16 (2 m) (.x) and h + 16 (2 m + 1) (.y)
+    // y[k][m]: token slot k, channels h + 16 (2 m) (.x) and h + 16 (2 m + 1) (.y).  Channel 16 i + h
+    // sits at 16 i + 4 (((h >> 2) & 3) ^ ((i >> 1) & 3)) + (h & 3) of its row (the swizzle of pass 1):
+    // for i = 2 q and 2 q + 1 the offset within the 16-channel group is off[q]
+    int off[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) off[q] = 4 * (((h >> 2) & 3) ^ q) + (h & 3);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int t = tg + 16 * (k ^ kown);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            y[k][q] = make_float2(sm.u.ys[t * kYStride + h + 32 * q], sm.u.ys[t * kYStride + h + 32 * q + 16]);
+            y[k][q] = make_float2(sm.u.ys[t * kYStride + 32 * q + off[q]], sm.u.ys[t * kYStride + 32 * q + 16 + off[q]]);
         if (rotate) {
             fwht_pairs<4>(y[k]);
 #pragma unroll
@@ -286,8 +289,16 @@ __device__ __forceinline__ void rotate_normalise(EncodeSmem& sm, const TileLanes
             const float2 t1 = token_sums(std::false_type(), no_shift8);
             const float mean = t1.x * (1.f / kTile);
             const float ms = t1.y * (1.f / kTile);
-            float var = ms - mean * mean;
-            if (__any_sync(0xffffffffu, var < kRedo * ms)) {  // warp-uniform
+            const float var = ms - mean * mean;
+            // the factors of the first pass go out at once; the warp vote on a mean-dominated row
+            // comes after them, off the path from the sums to the channel step
+            float b_new = var > kDegenerateRel * ms ? rsqrtf(var) : b_own;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float b = __shfl_sync(0xffffffffu, b_new, slot_src(k));
+                bb[k] = make_float2(b, b);
+            }
+            if (__any_sync(0xffffffffu, var < kRedo * ms)) {  // warp-uniform, rare
                 float2 sh[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -296,29 +307,32 @@ __device__ __forceinline__ void rotate_normalise(EncodeSmem& sm, const TileLanes
                 }
                 const float2 t2 = token_sums(std::true_type(), sh);
                 const float dm = t2.x * (1.f / kTile);
-                var = t2.y * (1.f / kTile) - dm * dm;
-            }
-            if (var > kDegenerateRel * ms) b_own = rsqrtf(var);
-        }
+                const float var2 = t2.y * (1.f / kTile) - dm * dm;
+                b_new = var2 > kDegenerateRel * ms ? rsqrtf(var2) : b_own;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float b = __shfl_sync(0xffffffffu, b_own, slot_src(k));
-            bb[k] = make_float2(b, b);
+                for (int k = 0; k < 8; ++k) {
+                    const float b = __shfl_sync(0xffffffffu, b_new, slot_src(k));
+                    bb[k] = make_float2(b, b);
+                }
+            }
+            b_own = b_new;
         }
+
         channel_sums(std::false_type(), no_shift4);
         __syncthreads();
-        float cms = 0.f;
+        float cms = 0.f, cmean = 0.f;
         bool redo = false;
         if (tid < kTile) {
             const float2 t = channel_total();
-            const float mean = t.x * (1.f / kTile);
+            cmean = t.x * (1.f / kTile);
             cms = t.y * (1.f / kTile);
-            const float var = cms - mean * mean;
+            const float var = cms - cmean * cmean;
             redo = var < kRedo * cms;
-            sm.u.late.cmean[tid] = mean;  // the shift of a second pass
             if (!redo && var > kDegenerateRel * cms) sm.cinv[tid] = rsqrtf(var);
         }
-        if (__syncthreads_or(redo)) {  // block-uniform: some column is dominated by its mean
+        if (__syncthreads_or(redo)) {  // block-uniform, rare: some column is dominated by its mean
+            if (tid < kTile) sm.u.late.cmean[tid] = cmean;  // the shift of the second pass
+            __syncthreads();
             float2 csh[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m)
