@@ -78,12 +78,21 @@ def ragged_dec_bytes(lens, Hq, Hkv, k_bits, v_bits):
     return cache, len(lens) * Hq * 128 * 2, len(lens) * Hq * 128 * 4
 
 
-def source_hash():
+# the sources each kernel's DRAM counters depend on (its own file and the headers it includes;
+# include/kvarn.h is added to every set)
+KERNEL_SOURCES = {
+    "kvarn_decode_attention": ("decode_attn.cu", "kvarn_common.cuh", "tcgen05.cuh", "kvarn_internal.h"),
+    "kvarn_encode_kv_blocks": ("encode.cu", "kvarn_common.cuh", "kvarn_internal.h"),
+}
+
+
+def source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_kvarn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    paths = [os.path.join(csrc, n) for n in KERNEL_SOURCES[kernel]] + [os.path.join(ROOT, "include", "kvarn.h")]
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -95,7 +104,7 @@ def ncu_traffic(kernel):
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 
@@ -218,11 +227,12 @@ def _ref_task(task):
 class OraclePool:
     """The fp64 oracle over every host core; step() runs one whole oracle step."""
 
-    def __init__(self):
+    def __init__(self, cores=None):
         import multiprocessing as mp
         from concurrent.futures import ProcessPoolExecutor
 
-        self.cores = len(os.sched_getaffinity(0))
+        avail = len(os.sched_getaffinity(0))
+        self.cores = avail if not cores else max(1, min(cores, avail))
         # one thread per worker: the cores are the parallelism (children inherit the environment)
         saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
         for k in saved:
@@ -254,7 +264,7 @@ class OraclePool:
         return (f"whole oracle steps: {ENC_SEQ * ENC_HKV} K + {ENC_SEQ * ENC_HKV} V tile encodes and "
                 f"{DEC_B * DEC_HKV} (sequence, kv head) decode units of {DEC_L} tokens x "
                 f"{DEC_HQ // DEC_HKV} query heads each, on a pool of {self.cores} single-threaded worker "
-                f"processes (one per host core); the decode cache's block tables cycle through "
+                f"processes (one per host core used); the decode cache's block tables cycle through "
                 f"{ORACLE_CACHE_BLOCKS} oracle-encoded blocks")
 
 
@@ -266,7 +276,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    pool = OraclePool()
+    pool = OraclePool(args.ref_cores)
     try:
         # whole steps: W warm-up and K timed, unless the box is so slow that they would not end in
         # about five minutes (then fewer timed steps, reported in `steps`)
@@ -787,6 +797,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-cores", type=int, default=0,
+                    help="reference arm: host cores for the oracle pool (default: all of them)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ctx", type=int, default=32768, help="decode context (profiling runs only)")
     ap.add_argument("--append-timing", action="store_true",

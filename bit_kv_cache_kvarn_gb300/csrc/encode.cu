@@ -56,30 +56,11 @@ struct EncodeSmem {
     float grp_inv_s1[kPadded];             // 1 / S1 (0 where S1 = 0)
     float grp_s1[kPadded];                 // S1
     float oth_inv_s2[kPadded];             // 1 / s2 along the other axis
-    float bred[kWarps];                    // block reductions
-    float bcast[4];
+    float bred[kWarps];                    // per-warp partial sums of the log factors
+    float2 bmax[kWarps];                   // per-warp partial maxima of (S, |m|) over the groups
     alignas(16) uint8_t params[KVARN_PARAM_BYTES];
     alignas(8) uint64_t bar;
 };
-
-__device__ __forceinline__ float block_sum_128(EncodeSmem& sm, float v, int tid) {
-    // sum of v over threads 0..127 (4 warps); result broadcast through shared memory
-    v = warp_sum(v);
-    if (tid < 128 && (tid & 31) == 0) sm.bred[tid >> 5] = v;
-    __syncthreads();
-    float r = sm.bred[0] + sm.bred[1] + sm.bred[2] + sm.bred[3];
-    __syncthreads();
-    return r;
-}
-
-__device__ __forceinline__ float block_max_128(EncodeSmem& sm, float v, int tid) {
-    v = warp_max(v);
-    if (tid < 128 && (tid & 31) == 0) sm.bred[tid >> 5] = v;
-    __syncthreads();
-    float r = fmaxf(fmaxf(sm.bred[0], sm.bred[1]), fmaxf(sm.bred[2], sm.bred[3]));
-    __syncthreads();
-    return r;
-}
 
 // Element (token slot k, channel h + 16 i) of a thread's rotated tile held as channel pairs.
 __device__ __forceinline__ float& yel(float2 (&y)[8][4], int k, int i) {
@@ -362,17 +343,32 @@ __device__ __forceinline__ void split_quantise_store(EncodeSmem& sm, const TileL
                                                      float* __restrict__ scale_out, int64_t otile, int rotate) {
     constexpr int kLevels = (1 << BITS) - 1;
     const int tid = L.tid, lane = L.lane, warp = L.warp, h = L.h, tsub = L.tsub, tg = L.tg, kown = L.kown;
-    (void)lane;
 
     // ---- scale split: s2 along the other axis (geometric mean 1, E4M3, clamped) ----
-    // K: other axis = token (factor r); V: other axis = channel (factor c).
+    // K: other axis = token (factor r, one lane of each lane pair h, h ^ 1 holds token
+    // tg + 16 kown); V: other axis = channel (factor c, channel tid for threads 0..127).  The log
+    // factors are summed per warp on the way into shared memory, so one barrier serves both.
+    float lf = 0.f;
     if (KIND == KVARN_KIND_K) {
-        if ((h & 1) == 0) sm.logf_[pad(tg + 16 * kown)] = -logf(b_own);
+        if ((h & 1) == 0) {
+            lf = -logf(b_own);
+            sm.logf_[pad(tg + 16 * kown)] = lf;
+        }
     } else {
-        if (tid < kTile) sm.logf_[pad(tid)] = -logf(sm.cinv[tid]);
+        if (tid < kTile) {
+            lf = -logf(sm.cinv[tid]);
+            sm.logf_[pad(tid)] = lf;
+        }
+    }
+    {
+        const float ws = warp_sum(lf);
+        if (lane == 0) sm.bred[warp] = ws;
     }
     __syncthreads();
-    const float mean_log = block_sum_128(sm, tid < kTile ? sm.logf_[pad(tid)] : 0.f, tid) * (1.f / kTile);
+    float log_sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) log_sum += sm.bred[w];
+    const float mean_log = log_sum * (1.f / kTile);
     if (tid < kTile) {
         float s2 = e4m3_value(e4m3_rn(expf(sm.logf_[pad(tid)] - mean_log)));
         s2 = fminf(fmaxf(s2, 0.001953125f), 448.f);  // [2^-9, 448]
@@ -421,6 +417,8 @@ __device__ __forceinline__ void split_quantise_store(EncodeSmem& sm, const TileL
             }
             sm.grp_min[pad(j)] = lo;
             sm.grp_scale[pad(j)] = (hi - lo) / (float)kLevels;
+            gmin_own = lo;
+            gmax_own = hi;
         }
     } else {
         float inv[8];
@@ -472,11 +470,26 @@ __device__ __forceinline__ void split_quantise_store(EncodeSmem& sm, const TileL
             sm.grp_scale[pad(t)] = (gmax_own - gmin_own) / (float)kLevels;
         }
     }
+    // per-warp maxima of S and |m| over the groups this warp's threads wrote (K: threads 0..127,
+    // V: the even lanes; every other thread contributes 0), read after the barrier below
+    {
+        const bool writer = (KIND == KVARN_KIND_K) ? tid < kTile : (h & 1) == 0;
+        float ms = writer ? (gmax_own - gmin_own) / (float)kLevels : 0.f;
+        float mm = writer ? fabsf(gmin_own) : 0.f;
+        ms = warp_max(ms);
+        mm = warp_max(mm);
+        if (lane == 0) sm.bmax[warp] = make_float2(ms, mm);
+    }
     __syncthreads();
 
     // ---- tile factor g, group scale S1 (E4M3, rounded up) and zero-point Z (FP16) ----
-    const float s_max = block_max_128(sm, tid < kTile ? sm.grp_scale[pad(tid)] : 0.f, tid);
-    const float m_max = block_max_128(sm, tid < kTile ? fabsf(sm.grp_min[pad(tid)]) : 0.f, tid);
+    float s_max = 0.f, m_max = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float2 bm = sm.bmax[w];
+        s_max = fmaxf(s_max, bm.x);
+        m_max = fmaxf(m_max, bm.y);
+    }
     const float g = tile_factor(s_max, m_max);
     const float inv_g = 1.f / g;  // exact: g is a power of two
     if (tid < kTile) {
@@ -592,7 +605,8 @@ __device__ __forceinline__ void split_quantise_store(EncodeSmem& sm, const TileL
                 reinterpret_cast<const uint4*>(sm.params)[tid];
         if (tid == 0) scale_out[otile] = g;
     }
-    __syncthreads();
+    // no barrier here: the next tile starts with the copy wait's barrier, before anything
+    // overwrites the packed rows or the parameters
 }
 
 // Initialises the copy barrier and starts the copy of the CTA's first tile (if any).

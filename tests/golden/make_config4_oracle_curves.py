@@ -7,6 +7,9 @@ Only the oracle (oracle/) and the seeded input generators run here; nothing come
 path.  It takes several minutes of CPU:
 
     python tests/golden/make_config4_oracle_curves.py
+
+With --time-only it runs the plain stack alone (reference and KVarN cache), prints the oracle's
+wall times and the host's CPU count as one JSON line and writes nothing.
 """
 from __future__ import annotations
 
@@ -50,6 +53,14 @@ def curves(kv_outliers: bool, codecs):
 
 
 def main():
+    if "--time-only" in sys.argv[1:]:
+        t0 = time.time()
+        r = curves(False, CODECS[:1])
+        print(json.dumps({"config4_plain_stack": {"reference_seconds": r["reference_seconds"],
+                                                   "kvarn_k2v2_seconds": r["kvarn_k2v2"]["seconds"],
+                                                   "total_seconds": round(time.time() - t0, 1),
+                                                   "host_cpus": len(os.sched_getaffinity(0))}}))
+        return
     res = {"config": dict(seed=SEED, layers=LAYERS, hidden=HIDDEN, hq=HQ, hkv=HKV, blocks=BLOCKS),
            "plain": curves(False, CODECS[:1]), "kv_outliers": curves(True, CODECS)}
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "config4_oracle_mae.json")

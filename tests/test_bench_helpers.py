@@ -50,10 +50,13 @@ def test_ncu_traffic_only_for_the_captured_sources(tmp_path, monkeypatch):
         committed = json.load(f)
     entry = committed["kvarn_decode_attention"]
     # the committed capture was taken on these sources: the bench reports it
-    if entry["source_hash"] == bench.source_hash():
+    if entry["source_hash"] == bench.source_hash("kvarn_decode_attention"):
         assert bench.ncu_traffic("kvarn_decode_attention") == entry["bytes_per_launch"]
+    # each kernel's hash covers its own sources only: the decode's does not change with the encoder
+    assert "encode.cu" not in bench.KERNEL_SOURCES["kvarn_decode_attention"]
+    assert "decode_attn.cu" not in bench.KERNEL_SOURCES["kvarn_encode_kv_blocks"]
     # a capture of other sources is not reported
-    monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "source_hash", lambda kernel: "0" * 16)
     assert bench.ncu_traffic("kvarn_decode_attention") is None
     assert bench.ncu_traffic("no_such_kernel") is None
 
