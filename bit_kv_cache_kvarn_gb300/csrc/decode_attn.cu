@@ -508,7 +508,7 @@ decode_split_kernel(DecodeArgs a) {
     float* einv = qrs + GH * kTile;                        // [8]
     float* mpart = einv + 8;                               // [4 warps][8]
     float* lpart = mpart + 32;                             // [4 warps][8]
-    float* zkpart = lpart + 32;                            // sum_j q'_j Z_j: [head] (GH <= 4) or [4 warps][8]
+    float* zkpart = lpart + 32;                            // sum_j q'_j Z_j: [head] or [4 warps][8]
     float* zvpart = zkpart + 32;                           // [4 warps][8] partial sum_t p Zv_t
     int* idring = reinterpret_cast<int*>(zvpart + 32);     // [kIdRing] tile ids (producer)
     uint8_t* cta = dsm + kWorkers * kWorkerStride;
@@ -673,6 +673,10 @@ decode_split_kernel(DecodeArgs a) {
         float m_run[GH], l_part[GH], o[GH];
         // the unit's rotated query for channel r and its scale, kept in registers for small groups
         constexpr bool kQReg = GH <= 4;
+        // sum_j q'_j Z_j of the score phase: with 2-bit K one warp per head (lane l: channels
+        // 4l..4l+3, one warp sum); otherwise per-warp partials of every head, combined after the
+        // barrier.  Measured: the first is ~1% faster at 2-bit K, ~3% slower at 4-bit K.
+        constexpr bool kZkPerHead = GH <= 4 && KB == 2;
         float qreg[kQReg ? GH : 1], ereg[kQReg ? GH : 1];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
@@ -710,7 +714,7 @@ decode_split_kernel(DecodeArgs a) {
                 load_row<KB>(sb + St::kK, r, x);
                 unpack_row_to_tmem<KB>(x, a_col + lane_off);
             }
-            if constexpr (GH <= 4) {
+            if constexpr (kZkPerHead) {
                 float xs[GH];
                 const float s1 = e4m3_value(sb[St::kKP + r]) * pre_k;
 #pragma unroll
@@ -736,12 +740,14 @@ decode_split_kernel(DecodeArgs a) {
                 const float z = fp16_value(reinterpret_cast<const uint16_t*>(sb + St::kKP + 256)[r]);
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    const float q = qv[h * kTile + r];
+                    float q;
+                    if constexpr (kQReg) q = qreg[h];
+                    else q = qv[h * kTile + r];
                     xs[h] = q * s1;
                     xz[h] = q * z;
                 }
                 store_b<GH>(bk, kk_k, xs);
-                // sum_j q'_j Z_j of eight heads: per-warp partials, combined after the barrier below
+                // sum_j q'_j Z_j: per-warp partials, combined after the barrier below
                 const float zsum = warp_sum_multi<GH>(xz, lane);
                 constexpr int kGroup = 32 / GH;
                 if ((lane & (kGroup - 1)) == 0) zkpart[wq * 8 + lane / kGroup] = zsum;
@@ -778,7 +784,7 @@ decode_split_kernel(DecodeArgs a) {
             float sc[GH], p[GH], zks[GH];
             const float tok = gk * e4m3_value(sb[St::kKP + 128 + r]);
             bool over = false;
-            if constexpr (GH <= 4) {
+            if constexpr (kZkPerHead) {
 #pragma unroll
                 for (int h = 0; h < GH; ++h) zks[h] = zkpart[h];
             } else {

@@ -99,24 +99,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 // (or kSpinLimit polls), sets *err_word and returns false; once *err_word is set by any thread of
 // the grid, every later wait returns false at once, so a stuck kernel ends within about a second.
 constexpr uint64_t kWaitNs = 1000000000ull;
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-constexpr int kFastPolls = 32;  // polls before the error word and the clock are consulted
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* err_word,
                                               uint64_t limit_ns) {
     const uint32_t addr = smem_addr(bar);
-    // Most waits end within a few polls (a tensor-core step, a copy issued long before); the first
-    // polls touch nothing but the barrier, so the error word's global load stays off that path.
-#pragma unroll 1
-    for (int f = 0; f < kFastPolls; ++f)
-        if (mbar_try_wait(addr, parity)) return true;
     uint64_t t0 = 0;
     for (long long i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
