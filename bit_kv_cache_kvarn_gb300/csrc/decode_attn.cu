@@ -673,10 +673,11 @@ decode_split_kernel(DecodeArgs a) {
         float m_run[GH], l_part[GH], o[GH];
         // the unit's rotated query for channel r and its scale, kept in registers for small groups
         constexpr bool kQReg = GH <= 4;
-        // sum_j q'_j Z_j of the score phase: with 2-bit K one warp per head (lane l: channels
-        // 4l..4l+3, one warp sum); otherwise per-warp partials of every head, combined after the
-        // barrier.  Measured: the first is ~1% faster at 2-bit K, ~3% slower at 4-bit K.
-        constexpr bool kZkPerHead = GH <= 4 && KB == 2;
+        // sum_j q'_j Z_j of the score phase: with 2-bit K and four heads one warp per head (lane l:
+        // channels 4l..4l+3, one warp sum); otherwise per-warp partials of every head, combined
+        // after the barrier.  Measured: the first is ~1% faster there, and 1-3% slower at 4-bit K
+        // or with one or two heads (where only that many warps would carry the sums).
+        constexpr bool kZkPerHead = GH == 4 && KB == 2;
         float qreg[kQReg ? GH : 1], ereg[kQReg ? GH : 1];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
