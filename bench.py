@@ -278,11 +278,11 @@ def run_reference(args):
         return
     pool = OraclePool(args.ref_cores)
     try:
-        # whole steps: W warm-up and K timed, unless the box is so slow that they would not end in
-        # about five minutes (then fewer timed steps, reported in `steps`)
+        # whole steps: W warm-up and K timed, unless the K steps would take more than about two
+        # minutes (then as many as fit, reported in `steps`, so the run ends within a few minutes)
         warm = [pool.step() for _ in range(args.warmup)]
         per = warm[-1][0]
-        n_timed = max(1, min(args.steps, int(300.0 / max(per, 1e-3))))
+        n_timed = max(1, min(args.steps, int(120.0 / max(per, 1e-3))))
         timed = [pool.step() for _ in range(n_timed)]
     finally:
         pool.close()
