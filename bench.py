@@ -204,7 +204,7 @@ def _ref_worker_init():
 
 
 def _ref_task(task):
-    """One piece of an oracle step; returns its CPU seconds."""
+    """One piece of an oracle step; returns (its kind, its CPU seconds)."""
     import numpy as np
 
     from oracle import kvarn_oracle as o
@@ -221,7 +221,7 @@ def _ref_task(task):
         tails = np.zeros((1, 1, 128, 128))
         q = _REF["q"][a:a + 1, b * group:(b + 1) * group]
         o.decode_attention(q, group, 1, *_REF["cache"], table, [DEC_L], tails, tails, 1 / math.sqrt(128), 2, 2)
-    return time.process_time() - t0
+    return kind, time.process_time() - t0
 
 
 class OraclePool:
@@ -252,10 +252,13 @@ class OraclePool:
         self.tasks += [("enc", a, min(n, a + ORACLE_ENC_CHUNK)) for a in range(0, n, ORACLE_ENC_CHUNK)]
 
     def step(self):
-        """(wall seconds, summed CPU seconds of the workers) of one whole step."""
+        """(wall seconds, summed CPU seconds of the workers) of one whole step; the CPU seconds of
+        the encodes and of the decode units are kept apart in self.last_split."""
         t0 = time.perf_counter()
-        cpu = sum(self.ex.map(_ref_task, self.tasks))
-        return time.perf_counter() - t0, cpu
+        parts = list(self.ex.map(_ref_task, self.tasks))
+        wall = time.perf_counter() - t0
+        self.last_split = {k: sum(c for kk, c in parts if kk == k) for k in ("enc", "dec")}
+        return wall, sum(c for _, c in parts)
 
     def close(self):
         self.ex.shutdown()
@@ -283,7 +286,10 @@ def run_reference(args):
         warm = [pool.step() for _ in range(args.warmup)]
         per = warm[-1][0]
         n_timed = max(1, min(args.steps, int(120.0 / max(per, 1e-3))))
-        timed = [pool.step() for _ in range(n_timed)]
+        timed, splits = [], []
+        for _ in range(n_timed):
+            timed.append(pool.step())
+            splits.append(pool.last_split)
     finally:
         pool.close()
     v = statistics.mean(w for w, _ in timed) * 1e6
@@ -296,7 +302,10 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": "CPU run"},
         "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": pool.cores, "kind": "oracle",
-                         "sample": sample, "cpu_seconds_per_step": round(cpu, 2)},
+                         "sample": sample, "cpu_seconds_per_step": round(cpu, 2),
+                         # single-threaded workers: the CPU seconds of each part are its one-core time
+                         "cpu_seconds_encode_config1": round(statistics.mean(x["enc"] for x in splits), 2),
+                         "cpu_seconds_decode_config2": round(statistics.mean(x["dec"] for x in splits), 2)},
         "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
