@@ -224,6 +224,13 @@ def _ref_task(task):
     return kind, time.process_time() - t0
 
 
+def pool_cores(requested=None):
+    """Worker count of the oracle pool: every host core this process may run on, or the requested
+    number clamped to 1..that."""
+    avail = len(os.sched_getaffinity(0))
+    return avail if not requested else max(1, min(int(requested), avail))
+
+
 class OraclePool:
     """The fp64 oracle over every host core; step() runs one whole oracle step."""
 
@@ -231,8 +238,7 @@ class OraclePool:
         import multiprocessing as mp
         from concurrent.futures import ProcessPoolExecutor
 
-        avail = len(os.sched_getaffinity(0))
-        self.cores = avail if not cores else max(1, min(cores, avail))
+        self.cores = pool_cores(cores)
         # one thread per worker: the cores are the parallelism (children inherit the environment)
         saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
         for k in saved:

@@ -84,3 +84,11 @@ def test_clock_summary_keeps_samples_of_the_timed_region(tmp_path):
     # no sampler: no clocks, said so
     c.proc = None
     assert bench.ClockSampler.summary(c, 0, 1)["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_oracle_pool_core_count():
+    avail = len(os.sched_getaffinity(0))
+    assert bench.pool_cores() == avail and bench.pool_cores(0) == avail
+    assert bench.pool_cores(1) == 1
+    assert bench.pool_cores(10 ** 6) == avail
+    assert bench.pool_cores(-3) == 1
