@@ -1301,7 +1301,10 @@ cudaError_t launch_decode(int k_bits, int v_bits, int group, const void* q, int 
     a.splits = plan.splits;
     a.piece = plan.piece;
     a.B = B;
-    const int gh = group;  // up to 8 heads x (hi, lo) fill the 16 MMA columns
+    // heads per unit: the largest of 8, 4, 2, 1 dividing the group (8 heads x (hi, lo) fill the 16
+    // MMA columns); a larger or odd group is cut into group / gh head blocks, each a unit of its own
+    // that reads the kv head's tiles again
+    const int gh = group % 8 == 0 ? 8 : (group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1));
     a.hblocks = group / gh;
     a.units = Hkv * a.hblocks;
     a.ws = static_cast<float*>(workspace);

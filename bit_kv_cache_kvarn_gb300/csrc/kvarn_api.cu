@@ -208,10 +208,7 @@ static kvarn_status check_decode_shape(const kvarn_config* cfg, int B, int Hq, i
     if (B < 0 || B > 65535) return fail(KVARN_ERR_INVALID_ARG, "B = %d outside 0..65535", B);
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
         return fail(KVARN_ERR_INVALID_ARG, "Hq = %d, Hkv = %d: need Hq a positive multiple of Hkv", Hq, Hkv);
-    const int g = Hq / Hkv;
-    if (g != 1 && g != 2 && g != 4 && g != 8)
-        return fail(KVARN_ERR_UNSUPPORTED, "Hq / Hkv = %d; supported: 1, 2, 4, 8", g);
-    if (Hkv * (g > 4 ? g / 4 : 1) > 65535) return fail(KVARN_ERR_INVALID_ARG, "Hkv = %d too large", Hkv);
+    if (Hq > 65535) return fail(KVARN_ERR_INVALID_ARG, "Hq = %d outside 1..65535", Hq);
     if (max_tiles < 0 || max_tiles > (1 << 24))
         return fail(KVARN_ERR_INVALID_ARG, "max_tiles = %d outside 0..2^24", max_tiles);
     return KVARN_OK;

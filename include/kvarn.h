@@ -180,8 +180,10 @@ size_t kvarn_decode_workspace_size(const kvarn_config* cfg, int B, int Hq, int H
  *   workspace   : at least kvarn_decode_workspace_size(...) bytes of device memory.
  *   out         : [B][Hq][128] float32 attention output (original basis); a sequence of
  *                 length 0 gets zeros.
- * Hq must be a multiple of Hkv with Hq/Hkv in {1, 2, 4, 8}.  Tile ids are not range-checked on
- * the device: they must index the pools the caller passes. */
+ * Hq must be a positive multiple of Hkv (Hq <= 65535).  The query heads of a kv head are taken in
+ * blocks of the largest of 8, 4, 2 and 1 that divides Hq/Hkv; each block reads the kv head's tiles
+ * once (so a group of 16 reads them twice, a group of 5 five times).  Tile ids are not range-checked
+ * on the device: they must index the pools the caller passes. */
 kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q_bf16, int B, int Hq,
                                     int Hkv, const void* k_codes, const void* k_params,
                                     const float* k_scale, const void* v_codes,

@@ -145,8 +145,10 @@ def test_sink_decode_validation_needs_no_gpu(lib):
 def test_decode_validation_needs_no_gpu(lib):
     cfg = _cfg()
     assert _decode(lib, cfg, Hq=6, Hkv=4) == 1
-    assert _decode(lib, cfg, Hq=12, Hkv=4) == 2  # group 3: unsupported
-    assert _decode(lib, cfg, Hq=32, Hkv=2) == 2  # group 16
+    # any whole group is accepted (B = 0: validated, nothing enqueued)
+    for hq, hkv in ((12, 4), (32, 2), (5, 1), (96, 8)):
+        assert _decode(lib, cfg, B=0, Hq=hq, Hkv=hkv) == 0, (hq, hkv)
+    assert _decode(lib, cfg, B=0, Hq=65536, Hkv=1) == 1
     assert _decode(lib, cfg, B=-1) == 1
     assert _decode(lib, cfg, max_tiles=-1) == 1
     assert _decode(lib, cfg, scale=float("inf")) == 1

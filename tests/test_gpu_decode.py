@@ -139,7 +139,10 @@ def test_many_sequences_and_many_slots(kv):
     print("151 slots worst rel-L2", check(gpu, oracle_out(cfg, q, 1, c, 0.09)))
 
 
-@pytest.mark.parametrize("k_bits,v_bits,hq,hkv", [(2, 2, 3, 3), (4, 4, 4, 2), (2, 4, 16, 2), (4, 2, 8, 1)])
+# groups 1, 2, 8 in one unit of heads; 12 = 3 blocks of 4, 16 = 2 blocks of 8, 6 = 3 blocks of 2,
+# 5 = 5 blocks of 1
+@pytest.mark.parametrize("k_bits,v_bits,hq,hkv", [(2, 2, 3, 3), (4, 4, 4, 2), (2, 4, 16, 2), (4, 2, 8, 1),
+                                                  (2, 2, 12, 1), (2, 2, 32, 2), (4, 2, 12, 2), (2, 4, 5, 1)])
 def test_group_sizes_and_bit_widths(kv, k_bits, v_bits, hq, hkv):
     cfg = kv.make_config(k_bits, v_bits, 8, 0)
     lens = [3 * 128 + 9, 20 * 128]
